@@ -1,0 +1,411 @@
+#!/usr/bin/env python
+"""Benchmark of one decode step over a block-paged KV cache on GB300.
+
+A step is the whole hot path for one batch: store the batch's new K/V tokens
+into the cache by slot_mapping (pkv_store_kvcache), then paged decode attention
+over every sequence's cached context (pkv_paged_decode: plan, split, combine).
+
+Default workload: 512 sequences, context lengths clip(rint(exp(ln 800 +
+N(0,1))), 16, 4096), 32 query / 8 KV heads, head_dim 128, block size 16, a
+fragmented pool; bf16, synthetic (seeded). One JSON line is printed by rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload decode_512seq|decode_64seq|decode_longtail|decode_3seq]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (weak
+scaling, no collective on the data path); the timed region is bracketed by a
+barrier and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode tokens/s + KV GB/s (% of GB300 HBM peak) at 512 seqs"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default="decode_512seq")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, enabled: bool = True):
+        self.enabled = enabled
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        if not self.enabled:
+            return self
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for _, _, flags in rows for k, v in enumerate(flags)
+                          if v.lower() == "active"})
+        sm = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# -------------------------------------------------------------- workloads --
+
+def make_workload(name, seed_offset=0, fill="device"):
+    from paged_kv_cache_86_gb300 import workloads as W
+    fn = W.NAMED[name]
+    import inspect
+    seed = inspect.signature(fn).parameters["seed"].default + seed_offset
+    return fn(seed=seed, fill=fill)
+
+
+def decode_bytes(w) -> int:
+    """Algorithmic HBM bytes of one decode launch: K and V of every cached token
+    once per KV head, q in, out, block-table entries and context lengths."""
+    hkv, hq, d, bs = w.num_kv_heads, w.num_q_heads, w.head_dim, w.block_size
+    ctx = w.context_lens.astype(np.int64)
+    return int((ctx * hkv * d * 2 * 2).sum() + w.num_seqs * hq * d * 2 * 2
+               + 4 * ((ctx + bs - 1) // bs).sum() + 4 * w.num_seqs)
+
+
+def store_bytes(w) -> int:
+    """K and V rows read from the new-token buffers and written to the cache, plus slots."""
+    return int(w.num_new_tokens * (2 * w.num_kv_heads * w.head_dim * 2 * 2 + 4))
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_source, name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(name)
+    if not rec or rec.get("source_sha256_16") != source_hash(kernel_source):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ cpu oracle --
+
+def cpu_oracle_sample(w, target_s=15.0, max_seqs=None):
+    """Time the oracle (store of the new tokens + decode) on a bounded sample of
+    the workload's sequences, on this host's cores. Returns a cpu_baseline dict."""
+    import torch
+    from oracle import attention as oracle
+    from paged_kv_cache_86_gb300.workloads import bf16_to_u16
+
+    cores = oracle.max_threads()
+    order = np.random.default_rng(0).permutation(w.num_seqs)
+    t = w.tensors
+    done_tokens, done_seqs, elapsed = 0, 0, 0.0
+    token_of_seq = np.cumsum(w.context_lens > 0) - 1
+    bs = w.block_size
+    batch = 8
+    while elapsed < target_s and done_seqs < w.num_seqs and (max_seqs is None or done_seqs < max_seqs):
+        ids = np.sort(order[done_seqs:done_seqs + batch])
+        rows = w.block_tables[ids]
+        nblk = [-(-int(w.context_lens[i]) // bs) for i in ids]
+        used = np.unique(np.concatenate([rows[j, :n] for j, n in enumerate(nblk)]))
+        remap = {int(b): k for k, b in enumerate(used)}
+        tables = np.full_like(rows, -1)
+        for j, n in enumerate(nblk):
+            tables[j, :n] = [remap[int(b)] for b in rows[j, :n]]
+        idx = torch.from_numpy(used.astype(np.int64)).to(t["k_cache"].device)
+        kc = bf16_to_u16(t["k_cache"].index_select(0, idx)).copy()
+        vc = bf16_to_u16(t["v_cache"].index_select(0, idx)).copy()
+        toks = token_of_seq[ids]
+        slots = np.array([remap[int(w.slot_mapping[k]) // bs] * bs + int(w.slot_mapping[k]) % bs
+                          for k in toks], np.int32)
+        key = bf16_to_u16(t["key"][torch.from_numpy(toks.astype(np.int64)).to(t["key"].device)])
+        val = bf16_to_u16(t["value"][torch.from_numpy(toks.astype(np.int64)).to(t["value"].device)])
+        q = bf16_to_u16(t["q"][torch.from_numpy(ids.astype(np.int64)).to(t["q"].device)])
+        lens = w.context_lens[ids].copy()
+        t0 = time.perf_counter()
+        oracle.store_kvcache(key, val, kc, vc, slots, bs)
+        oracle.paged_decode(q, kc, vc, tables, lens, w.scale)
+        elapsed += time.perf_counter() - t0
+        done_seqs += len(ids)
+        done_tokens += int(lens.sum())
+    value = done_seqs / elapsed if elapsed > 0 else None
+    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done_seqs} of {w.num_seqs} sequences ({done_tokens} cached tokens), "
+                      f"store + decode in fp64 C with OpenMP, {elapsed:.1f} s",
+            "seconds": elapsed}
+
+
+# --------------------------------------------------------------- GPU arm --
+
+def run_pkv(args, rank, world, device):
+    import torch
+    import torch.distributed as dist
+    import paged_kv_cache_86_gb300 as pkv
+    from paged_kv_cache_86_gb300 import _lib
+
+    torch.cuda.set_device(device)
+    w = make_workload(args.workload, seed_offset=rank, fill="device")
+    t = {k: v.to(device) for k, v in w.tensors.items()}
+    bt = torch.from_numpy(w.block_tables).to(device)
+    cl = torch.from_numpy(w.context_lens).to(device)
+    sm = torch.from_numpy(w.slot_mapping).to(device)
+    out = torch.empty_like(t["q"])
+    ws = torch.empty(pkv.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        pkv.store_kvcache(t["key"], t["value"], t["k_cache"], t["v_cache"], sm)
+        pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], bt, cl, w.scale, out=out, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if pkv.get_device_errors() != 0:
+        raise RuntimeError("device-side range check fired during warm-up")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    clocks = ClockSampler(device.index if device.index is not None else 0,
+                          enabled=(rank == 0 and not args.no_clocks))
+    with clocks:
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        step_ms = e0.elapsed_time(e1) / args.steps
+
+        # per-op durations over the same number of steps, events on the launching stream
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b, c in evs:
+            a.record(stream)
+            pkv.store_kvcache(t["key"], t["value"], t["k_cache"], t["v_cache"], sm)
+            b.record(stream)
+            pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], bt, cl, w.scale, out=out,
+                             workspace=ws)
+            c.record(stream)
+        torch.cuda.synchronize()
+    store_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
+    decode_ms = statistics.mean(b.elapsed_time(c) for _, b, c in evs)
+    if pkv.get_device_errors() != 0:
+        raise RuntimeError("device-side range check fired during the timed region")
+
+    if world > 1:
+        tt = torch.tensor([step_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        step_ms = float(tt.item())
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, store + decode, D2H of the output
+    host = {k: t[k].cpu().pin_memory() for k in ("q", "key", "value")}
+    host_meta = {"bt": bt.cpu().pin_memory(), "cl": cl.cpu().pin_memory(), "sm": sm.cpu().pin_memory()}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dev_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    dev_meta = {k: torch.empty_like(v, device=device) for k, v in host_meta.items()}
+    h2d = sum(v.numel() * v.element_size() for v in list(host.values()) + list(host_meta.values()))
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        for k in host_meta:
+            dev_meta[k].copy_(host_meta[k], non_blocking=True)
+        pkv.store_kvcache(dev_in["key"], dev_in["value"], t["k_cache"], t["v_cache"], dev_meta["sm"])
+        pkv.paged_decode(dev_in["q"], t["k_cache"], t["v_cache"], dev_meta["bt"], dev_meta["cl"],
+                         w.scale, out=out, workspace=ws)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / args.steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    peak, peak_kind = measured_peaks()
+    dbytes = decode_bytes(w)
+    achieved = dbytes / (decode_ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC, "value": world * w.num_seqs / (step_ms * 1e-3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, recipe in DESIGN.md)",
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "num_blocks": w.num_blocks,
+                   "total_context_tokens": int(w.context_lens.sum()),
+                   "kv_bytes_read_per_step": int((w.context_lens.astype(np.int64) * w.num_kv_heads * w.head_dim * 4).sum()),
+                   "l2": "inputs larger than L2: every step streams the whole KV context "
+                         f"({(w.context_lens.astype(np.int64) * w.num_kv_heads * w.head_dim * 4).sum() / 1e9:.2f} GB > 129 MB L2)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "kv_gbs": achieved,
+        "roofline": {"bound": "hbm", "kernel": "pkv_paged_decode (plan + split + combine)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": profiled_traffic(os.path.join(ROOT, "paged_kv_cache_86_gb300", "csrc",
+                                                              "decode.cu"), w.name),
+                     "algorithmic_bytes_per_launch": dbytes, "launch_ms": decode_ms},
+        "ops": {"store_ms": store_ms, "store_gbs": store_bytes(w) / (store_ms * 1e-3) / 1e9,
+                "decode_ms": decode_ms},
+        "e2e": {"value": world * w.num_seqs / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * 4,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_oracle_sample(w)
+    return result
+
+
+def run_reference(args, rank):
+    """The oracle, as it stands, on the host cores: the reference arm."""
+    if rank != 0:
+        return None
+    import torch
+    w = make_workload(args.workload, fill="device" if torch.cuda.is_available() else "host")
+    per_step = []
+    for _ in range(max(args.warmup, 0)):
+        cpu_oracle_sample(w, target_s=0.5, max_seqs=8)
+    samples = []
+    for _ in range(args.steps):
+        r = cpu_oracle_sample(w, target_s=max(1.0, 120.0 / max(args.steps, 1)), max_seqs=None)
+        samples.append(r)
+        per_step.append(r["value"])
+    value = statistics.mean(per_step)
+    secs = sum(r["seconds"] for r in samples)
+    cpu = {"value": value, "unit": UNIT, "cores": samples[0]["cores"], "kind": "oracle",
+           "sample": samples[0]["sample"] + f"; {len(samples)} steps, {secs:.1f} s total"}
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.num_seqs / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16)", "config": {"workload": w.name},
+            "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    device = torch.device("cuda", local)
+    from paged_kv_cache_86_gb300.build import build
+    if rank == 0:
+        build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    res = run_pkv(args, rank, world, device)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

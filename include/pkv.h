@@ -1,0 +1,186 @@
+/*
+ * pkv.h -- C ABI of libpkv: attention over a block-paged KV cache on one
+ * GB300 GPU (sm_103a).
+ *
+ * Three operations, whose arguments are the per-batch metadata fields that
+ * nano-vllm's attention Context carries (nano vllm代码详解, §2 context:
+ * is_prefill, cu_seqlens_q/k, max_seqlen_q/k, slot_mapping, context_lens,
+ * block_tables):
+ *
+ *   pkv_store_kvcache  write each new token's K and V into the cache slot
+ *                      named by slot_mapping;
+ *   pkv_paged_decode   one query per sequence over its context_lens[i] cached
+ *                      tokens, found through its block_tables row;
+ *   pkv_paged_prefill  varlen query chunks (cu_seqlens_q) over their cached
+ *                      prefix plus themselves (cu_seqlens_k), causal.
+ *
+ * Cache layout. One layer's K cache and V cache are two separate arrays of
+ * shape [num_blocks, block_size, num_kv_heads, head_dim], row-major, bf16.
+ * Logical block j of a sequence lives in physical block block_tables[i][j]
+ * (推理运行时, §分页 KV). Token p of a sequence is row p % block_size of
+ * physical block block_tables[i][p / block_size], and a flat slot is
+ * block_id * block_size + offset (the row-major index of a [num_blocks,
+ * block_size] table, as in Mini-SGLang 源码解析（二）§6.8).
+ *
+ * Index arrays are int32 (Mini-SGLang 源码解析（二）§7.8 keeps its page table
+ * in int32). Query head g reads KV head g / (num_q_heads / num_kv_heads).
+ *
+ * Ownership. The caller owns every buffer; all pointers except `stream` and
+ * host scalars are DEVICE pointers. The library allocates no device memory.
+ * Buffers that a call needs beyond its inputs and outputs (partial results of
+ * split sequences) come from a caller-provided workspace whose size the
+ * matching *_workspace_size function returns.
+ *
+ * Execution. Every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and never synchronises the host. A store must be
+ * ordered before the decode/prefill that reads the stored tokens, e.g. by
+ * issuing both on one stream.
+ *
+ * Errors. Arguments are validated on the host before anything is launched; a
+ * failed check returns a negative pkv_status and launches nothing. Device data
+ * (slots, block ids, lengths) is range-checked inside the kernels: an entry
+ * that is out of range is skipped (never dereferenced), its output is
+ * unspecified, and a bit is set in a per-device error word that
+ * pkv_get_device_errors() returns and clears.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_ARG = -1,       /* null pointer, negative size, misaligned pointer or stride */
+    PKV_ERR_SHAPE = -2,     /* head_dim / head counts / block size the kernels do not support */
+    PKV_ERR_DTYPE = -3,     /* dtype other than PKV_BF16 */
+    PKV_ERR_WORKSPACE = -4, /* workspace missing or smaller than *_workspace_size() */
+    PKV_ERR_CUDA = -5,      /* a CUDA runtime call failed (launch, attribute, copy) */
+    PKV_ERR_DEVICE = -6     /* a device-side range check fired (see pkv_get_device_errors) */
+} pkv_status;
+
+typedef enum { PKV_BF16 = 0 } pkv_dtype;
+
+/* Bits of the device error word. */
+#define PKV_DEVERR_SLOT 0x1u        /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_DEVERR_BLOCK_ID 0x2u    /* block_tables entry outside [0, num_blocks) */
+#define PKV_DEVERR_LENGTH 0x4u      /* a length beyond its table row or max_* bound, or negative */
+#define PKV_DEVERR_TIMEOUT 0x8u     /* an on-chip wait hit its iteration limit */
+
+/* ----------------------------------------------------------------- store --
+ * For t < num_tokens: slot = slot_mapping[t]; slot < 0 marks a padded token
+ * and writes nothing; otherwise block = slot / block_size, offset = slot %
+ * block_size, and key[t] (num_kv_heads * head_dim elements) is copied bit for
+ * bit to k_cache[block][offset], value[t] to v_cache[block][offset].
+ * (nano vllm代码详解 §2 context: slot_mapping; Mini-SGLang 源码解析（二）
+ * §6.7 writes each new token's page into the page table.)
+ *
+ *   key, value        token t's row starts at key + t * key_token_stride
+ *                     (elements), so K and V may be views into a fused QKV
+ *                     tensor; each row is num_kv_heads * head_dim contiguous
+ *                     elements. Rows and strides must be 16-byte aligned.
+ *   k_cache, v_cache  [num_blocks, block_size, num_kv_heads, head_dim], 16-byte aligned.
+ *   slot_mapping      [num_tokens] int32. Slots must be distinct (a duplicate
+ *                     slot leaves which token wins unspecified).
+ * head_dim * num_kv_heads must be a multiple of 8. num_tokens == 0 is a no-op.
+ */
+pkv_status pkv_store_kvcache(const void *key, const void *value,
+                             void *k_cache, void *v_cache,
+                             const int32_t *slot_mapping, int32_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t num_blocks,
+                             int64_t key_token_stride, int64_t value_token_stride,
+                             pkv_dtype dtype, void *stream);
+
+/* ---------------------------------------------------------------- decode --
+ * out[i, g, :] = softmax_p(scale * q[i, g, :] . K_i[p, g / G, :]) . V_i[p, g / G, :]
+ * over p < context_lens[i], where K_i[p] is row p % block_size of physical
+ * block block_tables[i * max_blocks_per_seq + p / block_size] and G =
+ * num_q_heads / num_kv_heads. The new token of a decode step is stored first
+ * and counts in context_lens[i]. A sequence with context_lens[i] == 0 gets a
+ * zero row. (nano vllm代码详解 §2 context: context_lens, block_tables;
+ * 推理运行时 §分页 KV: the kernel reads K/V through the mapping.)
+ *
+ *   out, q            [num_seqs, num_q_heads, head_dim] bf16, contiguous.
+ *   block_tables      [num_seqs, max_blocks_per_seq] int32; entries past
+ *                     ceil(context_lens[i] / block_size) are never read.
+ *   context_lens      [num_seqs] int32, each in [0, max_context_len] and
+ *                     max_context_len <= max_blocks_per_seq * block_size.
+ *   workspace         device buffer of at least
+ *                     pkv_decode_workspace_size(num_seqs, num_q_heads,
+ *                     num_kv_heads, head_dim) bytes, 256-byte aligned. Its
+ *                     contents need no initialisation and are scratch after
+ *                     the call; two calls in flight at once need two workspaces.
+ *   Supported: head_dim 128; num_kv_heads in {1, 2, 4, 8}; num_q_heads /
+ *   num_kv_heads in {1, 2, 4, 8}; any block_size >= 1; any scale.
+ * The work is split into equal token ranges over the GPU's SMs; a sequence that
+ * spans several ranges is finished by a log-sum-exp combine pass.
+ */
+size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim);
+
+pkv_status pkv_paged_decode(void *out, const void *q,
+                            const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *context_lens, int32_t num_seqs,
+                            int32_t max_context_len,
+                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks, float scale,
+                            void *workspace, size_t workspace_bytes,
+                            pkv_dtype dtype, void *stream);
+
+/* --------------------------------------------------------------- prefill --
+ * Sequence i owns query rows cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1 (q_len
+ * rows) and keys 0 .. k_len-1 with k_len = cu_seqlens_k[i+1] - cu_seqlens_k[i],
+ * read through its block_tables row. With causal != 0, query row r sits at
+ * absolute position (k_len - q_len) + r and attends to keys 0 .. (k_len -
+ * q_len) + r: a chunk follows its cached prefix (推理运行时 §Prefill 与
+ * decode 输入; Mini-SGLang 源码解析（二）§6.6 chunked prefill). The chunk's own
+ * K/V must already be stored (pkv_store_kvcache) before this call.
+ *
+ *   out, q            [total_q, num_q_heads, head_dim] bf16, contiguous,
+ *                     total_q = cu_seqlens_q[num_seqs].
+ *   cu_seqlens_q/k    [num_seqs + 1] int32, non-decreasing, starting at 0;
+ *                     q_len <= max_seqlen_q, k_len <= max_seqlen_k <=
+ *                     max_blocks_per_seq * block_size, and q_len <= k_len when causal.
+ *   workspace         at least pkv_prefill_workspace_size(...) bytes (0 today:
+ *                     NULL is accepted).
+ *   Supported: head_dim 128; num_q_heads / num_kv_heads in {1, 2, 4, 8};
+ *   block_size a multiple of 16 or a power of two >= 1 ... see DESIGN notes in
+ *   the implementation; unsupported shapes return PKV_ERR_SHAPE.
+ */
+size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t total_q,
+                                  int32_t num_q_heads, int32_t head_dim);
+
+pkv_status pkv_paged_prefill(void *out, const void *q,
+                             const void *k_cache, const void *v_cache,
+                             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                             int32_t max_seqlen_q, int32_t max_seqlen_k,
+                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                             int32_t num_seqs, int32_t total_q,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t num_blocks, float scale,
+                             int32_t causal, void *workspace, size_t workspace_bytes,
+                             pkv_dtype dtype, void *stream);
+
+/* ------------------------------------------------------------- utilities --
+ * pkv_get_device_errors: waits for `stream`, then returns (in *bits) and
+ * clears the error word of the current device. Returns PKV_ERR_DEVICE when any
+ * bit was set, PKV_OK otherwise, PKV_ERR_CUDA if the copy failed.
+ */
+pkv_status pkv_get_device_errors(void *stream, uint32_t *bits);
+
+const char *pkv_status_string(pkv_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

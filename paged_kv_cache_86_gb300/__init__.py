@@ -1,0 +1,13 @@
+"""Attention over a block-paged KV cache on one GB300 GPU.
+
+The compute path is the C-ABI library ``libpkv.so`` (hand-written sm_103a
+CUDA kernels, declared in ``include/pkv.h``); this package is its thin ctypes
+binding plus the seeded synthetic workload generator used by tests and the
+bench. Importing the package does not load the library; the first call does,
+and fails loudly if it has not been built.
+"""
+from ._lib import (PkvError, decode_workspace_size, get_device_errors, load, paged_decode,
+                   paged_prefill, prefill_workspace_size, store_kvcache, version)
+
+__all__ = ["PkvError", "decode_workspace_size", "get_device_errors", "load", "paged_decode",
+           "paged_prefill", "prefill_workspace_size", "store_kvcache", "version"]

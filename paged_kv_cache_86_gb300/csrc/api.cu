@@ -1,0 +1,236 @@
+// api.cu -- the extern "C" entry points of libpkv: host-side argument checks,
+// workspace sizing and kernel launches on the caller's stream. The contract of
+// each call is documented in include/pkv.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+__device__ uint32_t g_device_errors;  // PKV_DEVERR_* bits, one word per device
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t *g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+}  // namespace
+
+namespace pkv {
+
+uint32_t *device_error_word(cudaError_t *status) {
+  int dev = 0;
+  *status = cudaGetDevice(&dev);
+  if (*status != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *status = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    *status = cudaGetSymbolAddress(&p, g_device_errors);
+    if (*status != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<uint32_t *>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int sm_count(int device) {
+  if (device < 0 || device >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_sms[device] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) == cudaSuccess)
+      g_sms[device] = n;
+  }
+  return g_sms[device];
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_store_kvcache(const void *key, const void *value, void *k_cache, void *v_cache,
+                             const int32_t *slot_mapping, int32_t num_tokens,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             int32_t num_blocks, int64_t key_token_stride,
+                             int64_t value_token_stride, pkv_dtype dtype, void *stream) {
+  if (dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || num_blocks < 1)
+    return PKV_ERR_ARG;
+  const int64_t row = int64_t(num_kv_heads) * head_dim;
+  if (row % 8 != 0) return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ARG;
+  if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 != 0 ||
+      value_token_stride % 8 != 0)
+    return PKV_ERR_ARG;
+  cudaError_t e;
+  uint32_t *err = pkv::device_error_word(&e);
+  if (!err) return PKV_ERR_CUDA;
+  e = pkv::launch_store_kvcache(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                static_cast<int32_t>(row), key_token_stride, value_token_stride,
+                                int64_t(num_blocks) * block_size, err,
+                                static_cast<cudaStream_t>(stream));
+  return from_cuda(e);
+}
+
+size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim) {
+  if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim != 128) return 0;
+  cudaError_t e;
+  const int grid = pkv::decode_grid(num_q_heads, num_kv_heads, &e);
+  if (grid <= 0) return 0;
+  return pkv::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, grid);
+}
+
+pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *context_lens, int32_t num_seqs,
+                            int32_t max_context_len, int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                            void *workspace, size_t workspace_bytes, pkv_dtype dtype,
+                            void *stream) {
+  if (dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || block_size < 1 || num_blocks < 1 ||
+      max_blocks_per_seq < 0 || max_context_len < 0 || !std::isfinite(scale))
+    return PKV_ERR_ARG;
+  if (head_dim != 128) return PKV_ERR_SHAPE;
+  if (int64_t(max_context_len) > int64_t(max_blocks_per_seq) * block_size) return PKV_ERR_ARG;
+  if (int64_t(num_seqs) * max_context_len >= (int64_t(1) << 31)) return PKV_ERR_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !context_lens ||
+      (!block_tables && max_blocks_per_seq > 0))
+    return PKV_ERR_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ARG;
+  cudaError_t e;
+  const int grid = pkv::decode_grid(num_q_heads, num_kv_heads, &e);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  if (grid <= 0) return PKV_ERR_SHAPE;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < pkv::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, grid))
+    return PKV_ERR_WORKSPACE;
+  uint32_t *err = pkv::device_error_word(&e);
+  if (!err) return PKV_ERR_CUDA;
+  pkv::DecodeArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.max_context_len = max_context_len;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err = err;
+  return from_cuda(pkv::launch_paged_decode(a, grid, static_cast<cudaStream_t>(stream)));
+}
+
+size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                                  int32_t head_dim) {
+  (void)num_seqs;
+  (void)total_q;
+  (void)num_q_heads;
+  (void)head_dim;
+  return 0;
+}
+
+pkv_status pkv_paged_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                             int32_t max_seqlen_q, int32_t max_seqlen_k,
+                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                             int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             int32_t num_blocks, float scale, int32_t causal, void *workspace,
+                             size_t workspace_bytes, pkv_dtype dtype, void *stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (num_seqs < 0 || total_q < 0 || num_q_heads < 1 || num_kv_heads < 1 || block_size < 1 ||
+      num_blocks < 1 || max_blocks_per_seq < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
+      !std::isfinite(scale))
+    return PKV_ERR_ARG;
+  if (head_dim != 128) return PKV_ERR_SHAPE;
+  if (int64_t(max_seqlen_k) > int64_t(max_blocks_per_seq) * block_size) return PKV_ERR_ARG;
+  if (!pkv::prefill_supported(num_q_heads, num_kv_heads, block_size)) return PKV_ERR_SHAPE;
+  if (num_seqs == 0 || total_q == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_tables)
+    return PKV_ERR_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ARG;
+  cudaError_t e;
+  uint32_t *err = pkv::device_error_word(&e);
+  if (!err) return PKV_ERR_CUDA;
+  pkv::PrefillArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.cu_seqlens_q = cu_seqlens_q;
+  a.cu_seqlens_k = cu_seqlens_k;
+  a.max_seqlen_q = max_seqlen_q;
+  a.max_seqlen_k = max_seqlen_k;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.total_q = total_q;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.causal = causal;
+  a.err = err;
+  return from_cuda(pkv::launch_paged_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_get_device_errors(void *stream, uint32_t *bits) {
+  cudaError_t e;
+  uint32_t *err = pkv::device_error_word(&e);
+  if (!err) return PKV_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t host = 0;
+  if (cudaMemcpyAsync(&host, err, sizeof host, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(err, 0, sizeof host, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (bits) *bits = host;
+  return host ? PKV_ERR_DEVICE : PKV_OK;
+}
+
+const char *pkv_status_string(pkv_status status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_ARG: return "invalid argument";
+    case PKV_ERR_SHAPE: return "unsupported shape";
+    case PKV_ERR_DTYPE: return "unsupported dtype";
+    case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case PKV_ERR_CUDA: return "CUDA runtime error";
+    case PKV_ERR_DEVICE: return "device-side range check fired";
+  }
+  return "unknown status";
+}
+
+int32_t pkv_version(void) { return 100; }
+
+}  // extern "C"

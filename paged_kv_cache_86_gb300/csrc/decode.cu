@@ -1,0 +1,667 @@
+// decode.cu -- split-context paged decode attention for GB300 (sm_103a).
+//
+// One query token per sequence attends to its context_lens[i] cached tokens,
+// read through its block_tables row (nano vllm代码详解 §2 context;
+// 推理运行时 §分页 KV: logical block j -> physical block b_j). Decode is bound
+// by reading the KV cache (Mini-SGLang 源码解析（二）§8.3: decode is
+// memory-bound on KV cache reads), so the design goal is to stream every K/V
+// byte exactly once at full HBM bandwidth with all SMs busy whatever the
+// length mix.
+//
+// Three launches on the caller's stream:
+//   1. plan     one CTA: prefix sums cu[i] of the (range-checked) context
+//               lengths and the token-range size W = ceil(total / grid)
+//               (rounded up to 16, at least 64).
+//   2. split    a persistent grid of `grid` CTAs (every SM, as many CTAs as
+//               fit). CTA b owns the flat token range [b*W, (b+1)*W) of the
+//               concatenated contexts, so every CTA streams the same number
+//               of bytes however long or short the sequences are. Inside a
+//               CTA, one producer warp walks the range sequence by sequence
+//               and block by block and moves each run of up to
+//               16 KB / (Hkv*256 B) tokens of one physical block into a
+//               shared-memory stage with two bulk TMA copies (K and V; a
+//               run of one block is contiguous across all KV heads in the
+//               [NB, bs, Hkv, D] layout). Eight consumer warps each take one
+//               KV head and an 8-token slice of the stage: the G query heads
+//               of the group are scored together (K is read from shared
+//               memory once per group), scores are reduced across the 16
+//               lanes of a half-warp with a reduce-scatter of shuffles, the
+//               online softmax (base 2; q is pre-scaled by scale*log2 e) is
+//               updated once per stage, and P*V is accumulated with packed
+//               fp32x2 FMAs. A sequence wholly inside one range is
+//               normalised and written as bf16 directly; a sequence cut by a
+//               range boundary leaves a partial (o/l, m, l) for each of its
+//               pieces.
+//   3. combine  one CTA per sequence merges the partials of cut sequences
+//               with the log-sum-exp rule  M = max m_s,
+//               o = sum_s l_s 2^(m_s - M) o_s / sum_s l_s 2^(m_s - M),
+//               and writes zero rows for empty sequences.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kHeadDim = 128;
+constexpr int kHeadBytes = kHeadDim * 2;      // one token of one KV head, bf16
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 3;
+constexpr int kStageBytes = 32768;            // K half + V half
+constexpr int kTokensPerWarp = 8;             // stage tokens per consumer warp
+constexpr int kMinRange = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned kFull = 0xffffffffu;
+
+enum : int { kFirst = 1, kLast = 2, kEnd = 4, kSkip = 8 };
+
+struct StageDesc {
+  int seq, pos, ntok, flags, slot, pad0, pad1, pad2;
+};
+
+// Workspace: a 256-byte header, cu[S+1], then the partial results.
+struct Header {
+  int total;   // sum of clamped context lengths
+  int range;   // tokens per CTA range (W)
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t cu, ml, o, total;
+  int entries;  // partial (o, m, l) records per query head
+};
+
+__host__ __device__ inline WsLayout ws_layout(int num_seqs, int num_q_heads, int wph, int grid) {
+  WsLayout l;
+  l.cu = 256;
+  const int entries = 2 * grid * wph + (wph > 1 ? num_seqs * wph : 0);
+  l.entries = entries;
+  l.ml = align256(l.cu + sizeof(int) * (size_t(num_seqs) + 1));
+  l.o = align256(l.ml + sizeof(float2) * size_t(entries) * num_q_heads);
+  l.total = align256(l.o + sizeof(float) * size_t(entries) * num_q_heads * kHeadDim);
+  return l;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------------ plan --
+
+__global__ void __launch_bounds__(1024)
+decode_plan_kernel(const int32_t *__restrict__ context_lens, int num_seqs, int max_context_len,
+                   int grid, uint8_t *ws, uint32_t *err) {
+  __shared__ int warp_sums[32];
+  __shared__ int base;
+  int *cu = reinterpret_cast<int *>(ws + 256);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    base = 0;
+    cu[0] = 0;
+  }
+  __syncthreads();
+  for (int start = 0; start < num_seqs; start += 1024) {
+    const int i = start + threadIdx.x;
+    int x = 0;
+    if (i < num_seqs) {
+      x = context_lens[i];
+      if (x < 0 || x > max_context_len) {
+        raise_error(err, PKV_DEVERR_LENGTH);
+        x = x < 0 ? 0 : max_context_len;
+      }
+    }
+    int v = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(kFull, v, off);
+      if (lane >= off) v += y;
+    }
+    if (lane == 31) warp_sums[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(kFull, w, off);
+        if (lane >= off) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int incl = v + (warp > 0 ? warp_sums[warp - 1] : 0);
+    if (i < num_seqs) cu[i + 1] = base + incl;
+    __syncthreads();
+    if (threadIdx.x == 1023) base += incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    Header *h = reinterpret_cast<Header *>(ws);
+    const int total = base;
+    int range = (total + grid - 1) / grid;
+    range = (range + 15) / 16 * 16;
+    h->total = total;
+    h->range = range < kMinRange ? kMinRange : range;
+  }
+}
+
+// ----------------------------------------------------------------- split --
+
+struct SplitParams {
+  __nv_bfloat16 *out;
+  const __nv_bfloat16 *q;
+  const uint8_t *k_cache;
+  const uint8_t *v_cache;
+  const int32_t *block_tables;
+  int max_blocks_per_seq;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int block_size;
+  int num_blocks;
+  float qscale;  // scale * log2(e)
+  const uint8_t *ws;
+  float2 *ml;    // partial (m, l) records
+  float *po;     // partial normalised outputs
+  uint32_t *err;
+};
+
+template <int G>
+struct GroupTraits {
+  static constexpr int kLogG = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  static constexpr int kScatterShift = 4 - kLogG;  // head of a lane after the reduce-scatter
+};
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, G <= 4 ? 2 : 1)
+decode_split_kernel(const SplitParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t *stage_base = smem;
+  uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+  uint64_t *empty_bar = full_bar + kStages;
+  StageDesc *desc = reinterpret_cast<StageDesc *>(empty_bar + kStages);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(desc + kStages);
+  float *score_buf = reinterpret_cast<float *>(desc + kStages) + 32;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Header hdr = *reinterpret_cast<const Header *>(p.ws);
+  const int *cu = reinterpret_cast<const int *>(p.ws + 256);
+  const int lo = static_cast<int>(blockIdx.x) * hdr.range;
+  const int hi = min(lo + hdr.range, hdr.total);
+  const int row_bytes = p.num_kv_heads * kHeadBytes;
+  const int wph = kConsumerWarps / p.num_kv_heads;  // consumer warps per KV head
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), kConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    const int stage_tokens = (kStageBytes / 2) / row_bytes;
+    const uint64_t policy = l2_policy_evict_first();
+    int issued = 0;
+    bool ok = true;
+
+    // Arms one stage; returns false (and arms nothing) once waiting for a free
+    // stage has given up.
+    auto issue = [&](int seq, int pos, int ntok, int flags, int slot, int blk, int off) {
+      const int s = issued % kStages;
+      const uint32_t round = static_cast<uint32_t>(issued / kStages);
+      int good = 1;
+      if (lane == 0) {
+        if (round > 0 && !mbar_wait(smem_addr(&empty_bar[s]), (round - 1) & 1, abort_flag)) {
+          good = 0;
+          *abort_flag = 1;
+          raise_error(p.err, PKV_DEVERR_TIMEOUT);
+        } else {
+          const bool valid = (flags & kEnd) == 0 && blk >= 0 && blk < p.num_blocks;
+          if ((flags & kEnd) == 0 && !valid) {
+            flags |= kSkip;
+            raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+          }
+          StageDesc d;
+          d.seq = seq; d.pos = pos; d.ntok = ntok; d.flags = flags; d.slot = slot;
+          d.pad0 = d.pad1 = d.pad2 = 0;
+          desc[s] = d;
+          const uint32_t fb = smem_addr(&full_bar[s]);
+          if (valid) {
+            const uint32_t bytes = static_cast<uint32_t>(ntok * row_bytes);
+            mbar_arrive_expect_tx(fb, 2 * bytes);
+            const size_t src = (static_cast<size_t>(blk) * p.block_size + off) * row_bytes;
+            const uint32_t dst = smem_addr(stage_base + s * kStageBytes);
+            bulk_g2s(dst, p.k_cache + src, bytes, fb, policy);
+            bulk_g2s(dst + kStageBytes / 2, p.v_cache + src, bytes, fb, policy);
+          } else {
+            mbar_arrive(fb);
+          }
+        }
+      }
+      good = __shfl_sync(kFull, good, 0);
+      if (good) ++issued;
+      return good != 0;
+    };
+
+    if (lo < hi) {
+      // first sequence whose tokens reach past lo
+      int a = 0, b = p.num_seqs - 1;
+      while (a < b) {
+        const int m = (a + b) >> 1;
+        if (cu[m + 1] > lo) b = m; else a = m + 1;
+      }
+      for (int i = a; ok && i < p.num_seqs; ++i) {
+        const int c0 = cu[i], c1 = cu[i + 1];
+        if (c0 >= hi) break;
+        if (c1 == c0) continue;
+        const int seg_lo = max(lo, c0) - c0;
+        const int seg_hi = min(hi, c1) - c0;
+        const bool complete = c0 >= lo && c1 <= hi;
+        const int slot = complete ? -1 : (c0 <= lo ? 2 * int(blockIdx.x) : 2 * int(blockIdx.x) + 1);
+        const int32_t *row = p.block_tables + static_cast<size_t>(i) * p.max_blocks_per_seq;
+        int cached = -1 << 30, my_id = -1;
+        bool first = true;
+        for (int pos = seg_lo; ok && pos < seg_hi;) {
+          const int lb = pos / p.block_size;
+          const int off = pos - lb * p.block_size;
+          const int ntok = min(min(stage_tokens, p.block_size - off), seg_hi - pos);
+          if (lb < cached || lb >= cached + 32) {  // refill the window of 32 block ids
+            cached = lb;
+            my_id = lb + lane < p.max_blocks_per_seq ? __ldg(row + lb + lane) : -1;
+          }
+          const int blk = __shfl_sync(kFull, my_id, lb - cached);
+          const int flags = (first ? kFirst : 0) | (pos + ntok == seg_hi ? kLast : 0);
+          first = false;
+          ok = issue(i, pos, ntok, flags, slot, blk, off);
+          pos += ntok;
+        }
+      }
+    }
+    if (ok) ok = issue(0, 0, 0, kEnd, -1, 0, 0);
+    // Drain: every copy this CTA issued must land before its shared memory goes away.
+    if (lane == 0) {
+      const int first = issued > kStages ? issued - kStages : 0;
+      for (int k = first; k < issued; ++k)
+        mbar_wait(smem_addr(&full_bar[k % kStages]), (k / kStages) & 1, nullptr);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  using Tr = GroupTraits<G>;
+  const int head = warp % p.num_kv_heads;
+  const int sub = warp / p.num_kv_heads;
+  const int hf = lane >> 4;
+  const int l16 = lane & 15;
+  const int my_head_after_scatter = l16 >> Tr::kScatterShift;
+  const bool score_writer = (l16 & ((16 / G) - 1)) == 0;
+  const int own_g = lane & (G - 1);  // head whose score sum this lane keeps
+  float *sc = score_buf + warp * kTokensPerWarp * G;
+
+  float2 q2[G][4];
+  float2 acc[G][4];
+  float m_run[G];
+  float l_part = 0.f;
+
+  for (int k = 0;; ++k) {
+    const int s = k % kStages;
+    if (!mbar_wait(smem_addr(&full_bar[s]), (k / kStages) & 1, abort_flag)) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        raise_error(p.err, PKV_DEVERR_TIMEOUT);
+      }
+      break;
+    }
+    const StageDesc d = desc[s];
+    if (d.flags & kEnd) break;
+
+    if (d.flags & kFirst) {
+      const uint4 *qrow = reinterpret_cast<const uint4 *>(
+          p.q + (static_cast<size_t>(d.seq) * p.num_q_heads + head * G) * kHeadDim);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const uint4 raw = __ldg(qrow + g * (kHeadDim / 8) + l16);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float2 f = bf16x2_to_float2(w[c]);
+          q2[g][c] = make_float2(f.x * p.qscale, f.y * p.qscale);
+          acc[g][c] = make_float2(0.f, 0.f);
+        }
+        m_run[g] = -INFINITY;
+      }
+      l_part = 0.f;
+    }
+
+    const int t0 = sub * kTokensPerWarp;
+    const int nw = (d.flags & kSkip) ? 0 : min(max(d.ntok - t0, 0), kTokensPerWarp);
+    if (nw > 0) {
+      const uint32_t kb = smem_addr(stage_base + s * kStageBytes) + t0 * row_bytes +
+                          head * kHeadBytes + l16 * 16;
+      const uint32_t vb = kb + kStageBytes / 2;
+
+      // scores of this warp's tokens, two tokens (one per half-warp) at a time
+      for (int it = 0; it < (nw + 1) >> 1; ++it) {
+        const int j = 2 * it + hf;
+        const uint4 kr = lds128(kb + j * row_bytes);
+        const float2 k0 = bf16x2_to_float2(kr.x), k1 = bf16x2_to_float2(kr.y);
+        const float2 k2 = bf16x2_to_float2(kr.z), k3 = bf16x2_to_float2(kr.w);
+        float sv[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float2 a2 = fmul2(q2[g][0], k0);
+          a2 = ffma2(q2[g][1], k1, a2);
+          a2 = ffma2(q2[g][2], k2, a2);
+          a2 = ffma2(q2[g][3], k3, a2);
+          sv[g] = a2.x + a2.y;
+        }
+        // reduce-scatter over the 16 lanes of the half-warp: each level halves
+        // the heads a lane keeps and adds its partner's copy of them
+#pragma unroll
+        for (int n = G, off = 8; n > 1; n >>= 1, off >>= 1) {
+          const bool up = (lane & off) != 0;
+#pragma unroll
+          for (int i2 = 0; i2 < n / 2; ++i2) {
+            const float send = up ? sv[i2] : sv[i2 + n / 2];
+            const float keep = up ? sv[i2 + n / 2] : sv[i2];
+            sv[i2] = keep + __shfl_xor_sync(kFull, send, off);
+          }
+        }
+#pragma unroll
+        for (int off = 8 >> Tr::kLogG; off >= 1; off >>= 1)
+          sv[0] += __shfl_xor_sync(kFull, sv[0], off);
+        if (j < nw && score_writer) sc[j * G + my_head_after_scatter] = sv[0];
+      }
+      __syncwarp();
+
+      // online softmax update, once per stage: entry e = token * G + head
+      const int ne = nw * G;
+      const float v0 = lane < ne ? sc[lane] : -INFINITY;
+      const float v1 = (G == 8 && lane + 32 < ne) ? sc[lane + 32] : -INFINITY;
+      float mx = fmaxf(v0, v1);
+#pragma unroll
+      for (int off = 16; off >= G; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+      float alpha[G];
+      float m_own = 0.f, alpha_own = 1.f;
+      bool rescale = false;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float stage_max = __shfl_sync(kFull, mx, g);
+        const float m_new = fmaxf(m_run[g], stage_max);
+        alpha[g] = fast_exp2(m_run[g] - m_new);
+        rescale |= alpha[g] != 1.f;
+        m_run[g] = m_new;
+        if (own_g == g) {
+          m_own = m_new;
+          alpha_own = alpha[g];
+        }
+      }
+      const float p0 = lane < ne ? fast_exp2(v0 - m_own) : 0.f;
+      const float p1 = (G == 8 && lane + 32 < ne) ? fast_exp2(v1 - m_own) : 0.f;
+      if (lane < ne) sc[lane] = p0;
+      if (G == 8 && lane + 32 < ne) sc[lane + 32] = p1;
+      l_part = l_part * alpha_own + p0 + p1;
+      if (rescale) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float2 a2 = make_float2(alpha[g], alpha[g]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[g][c] = fmul2(acc[g][c], a2);
+        }
+      }
+      __syncwarp();
+
+      // P * V
+      for (int j = hf; j < nw; j += 2) {
+        const uint4 vr = lds128(vb + j * row_bytes);
+        const float2 v0f = bf16x2_to_float2(vr.x), v1f = bf16x2_to_float2(vr.y);
+        const float2 v2f = bf16x2_to_float2(vr.z), v3f = bf16x2_to_float2(vr.w);
+        float pj[G];
+        if constexpr (G == 1) {
+          pj[0] = sc[j];
+        } else if constexpr (G == 2) {
+          const float2 t = *reinterpret_cast<const float2 *>(sc + j * 2);
+          pj[0] = t.x; pj[1] = t.y;
+        } else {
+#pragma unroll
+          for (int g4 = 0; g4 < G; g4 += 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(sc + j * G + g4);
+            pj[g4] = t.x; pj[g4 + 1] = t.y; pj[g4 + 2] = t.z; pj[g4 + 3] = t.w;
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float2 pp = make_float2(pj[g], pj[g]);
+          acc[g][0] = ffma2(pp, v0f, acc[g][0]);
+          acc[g][1] = ffma2(pp, v1f, acc[g][1]);
+          acc[g][2] = ffma2(pp, v2f, acc[g][2]);
+          acc[g][3] = ffma2(pp, v3f, acc[g][3]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
+
+    if (d.flags & kLast) {
+      // fold the two half-warps and the per-lane softmax sums
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          acc[g][c].x += __shfl_xor_sync(kFull, acc[g][c].x, 16);
+          acc[g][c].y += __shfl_xor_sync(kFull, acc[g][c].y, 16);
+        }
+      float lt = l_part;
+#pragma unroll
+      for (int off = 16; off >= G; off >>= 1) lt += __shfl_xor_sync(kFull, lt, off);
+      float l_sum[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) l_sum[g] = __shfl_sync(kFull, lt, g);
+
+      if (wph == 1 && d.slot < 0) {
+        if (hf == 0) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float inv = l_sum[g] > 0.f ? 1.f / l_sum[g] : 0.f;
+            uint4 o;
+            o.x = float2_to_bf16x2(acc[g][0].x * inv, acc[g][0].y * inv);
+            o.y = float2_to_bf16x2(acc[g][1].x * inv, acc[g][1].y * inv);
+            o.z = float2_to_bf16x2(acc[g][2].x * inv, acc[g][2].y * inv);
+            o.w = float2_to_bf16x2(acc[g][3].x * inv, acc[g][3].y * inv);
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                p.out + (static_cast<size_t>(d.seq) * p.num_q_heads + head * G + g) * kHeadDim);
+            dst[l16] = o;
+          }
+        }
+      } else {
+        const int entry = d.slot >= 0 ? d.slot * wph + sub
+                                      : 2 * int(gridDim.x) * wph + d.seq * wph + sub;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const int qh = head * G + g;
+          const size_t rec = static_cast<size_t>(entry) * p.num_q_heads + qh;
+          const float inv = l_sum[g] > 0.f ? 1.f / l_sum[g] : 0.f;
+          if (hf == 0) {
+            float4 *dst = reinterpret_cast<float4 *>(p.po + rec * kHeadDim) + l16 * 2;
+            dst[0] = make_float4(acc[g][0].x * inv, acc[g][0].y * inv, acc[g][1].x * inv,
+                                 acc[g][1].y * inv);
+            dst[1] = make_float4(acc[g][2].x * inv, acc[g][2].y * inv, acc[g][3].x * inv,
+                                 acc[g][3].y * inv);
+          }
+          if (lane == 0) p.ml[rec] = make_float2(m_run[g], l_sum[g]);
+        }
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------- combine --
+
+struct CombineParams {
+  __nv_bfloat16 *out;
+  const uint8_t *ws;
+  const float2 *ml;
+  const float *po;
+  int num_seqs;
+  int num_q_heads;
+  int wph;
+  int grid;
+};
+
+__global__ void __launch_bounds__(128) decode_combine_kernel(const CombineParams p) {
+  const int i = blockIdx.x;
+  const Header hdr = *reinterpret_cast<const Header *>(p.ws);
+  const int *cu = reinterpret_cast<const int *>(p.ws + 256);
+  const int c0 = cu[i], c1 = cu[i + 1];
+  __nv_bfloat16 *orow = p.out + static_cast<size_t>(i) * p.num_q_heads * kHeadDim;
+  const int items = p.num_q_heads * (kHeadDim / 4);
+  if (c1 == c0) {  // empty context: zero row
+    for (int x = threadIdx.x; x < items; x += blockDim.x)
+      reinterpret_cast<uint2 *>(orow)[x] = make_uint2(0u, 0u);
+    return;
+  }
+  const int b_first = c0 / hdr.range;
+  const int b_last = (c1 - 1) / hdr.range;
+  if (p.wph == 1 && b_first == b_last) return;  // written by the split kernel
+  for (int x = threadIdx.x; x < items; x += blockDim.x) {
+    const int qh = x / (kHeadDim / 4);
+    const int d4 = x % (kHeadDim / 4);
+    float m_max = -INFINITY;
+    for (int b = b_first; b <= b_last; ++b) {
+      const int base = b_first == b_last ? 2 * p.grid * p.wph + i * p.wph
+                                         : ((b == b_first && c0 > b * hdr.range) ? 2 * b + 1 : 2 * b) * p.wph;
+      for (int w = 0; w < p.wph; ++w)
+        m_max = fmaxf(m_max, p.ml[static_cast<size_t>(base + w) * p.num_q_heads + qh].x);
+    }
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l_tot = 0.f;
+    if (m_max != -INFINITY) {
+      for (int b = b_first; b <= b_last; ++b) {
+        const int base = b_first == b_last ? 2 * p.grid * p.wph + i * p.wph
+                                           : ((b == b_first && c0 > b * hdr.range) ? 2 * b + 1 : 2 * b) * p.wph;
+        for (int w = 0; w < p.wph; ++w) {
+          const size_t rec = static_cast<size_t>(base + w) * p.num_q_heads + qh;
+          const float2 ml = p.ml[rec];
+          const float wgt = ml.y * fast_exp2(ml.x - m_max);
+          const float4 v = reinterpret_cast<const float4 *>(p.po + rec * kHeadDim)[d4];
+          o.x += wgt * v.x; o.y += wgt * v.y; o.z += wgt * v.z; o.w += wgt * v.w;
+          l_tot += wgt;
+        }
+      }
+    }
+    const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+    uint2 packed;
+    packed.x = float2_to_bf16x2(o.x * inv, o.y * inv);
+    packed.y = float2_to_bf16x2(o.z * inv, o.w * inv);
+    reinterpret_cast<uint2 *>(orow)[x] = packed;
+  }
+}
+
+size_t split_smem_bytes(int group) {
+  return size_t(kStages) * kStageBytes + 2 * kStages * sizeof(uint64_t) +
+         kStages * sizeof(StageDesc) + 32 * sizeof(float) +
+         size_t(kConsumerWarps) * kTokensPerWarp * group * sizeof(float);
+}
+
+template <int G>
+cudaError_t prepare_split(int *ctas_per_sm) {
+  const size_t smem = split_smem_bytes(G);
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_split_kernel<G>,
+                                                       kThreads, smem);
+}
+
+bool supported_heads(int num_q_heads, int num_kv_heads) {
+  if (num_kv_heads != 1 && num_kv_heads != 2 && num_kv_heads != 4 && num_kv_heads != 8) return false;
+  if (num_q_heads % num_kv_heads != 0) return false;
+  const int g = num_q_heads / num_kv_heads;
+  return g == 1 || g == 2 || g == 4 || g == 8;
+}
+
+}  // namespace
+
+int decode_grid(int num_q_heads, int num_kv_heads, cudaError_t *status) {
+  *status = cudaSuccess;
+  if (!supported_heads(num_q_heads, num_kv_heads)) return 0;
+  int dev = 0;
+  if ((*status = cudaGetDevice(&dev)) != cudaSuccess) return 0;
+  int per_sm = 0;
+  switch (num_q_heads / num_kv_heads) {
+    case 1: *status = prepare_split<1>(&per_sm); break;
+    case 2: *status = prepare_split<2>(&per_sm); break;
+    case 4: *status = prepare_split<4>(&per_sm); break;
+    default: *status = prepare_split<8>(&per_sm); break;
+  }
+  if (*status != cudaSuccess || per_sm < 1) return 0;
+  return per_sm * sm_count(dev);
+}
+
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int grid) {
+  const int wph = kConsumerWarps / num_kv_heads;
+  return ws_layout(num_seqs, num_q_heads, wph, grid).total;
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs &a, int grid, cudaStream_t stream) {
+  if (a.num_seqs == 0) return cudaSuccess;
+  const int wph = kConsumerWarps / a.num_kv_heads;
+  const int group = a.num_q_heads / a.num_kv_heads;
+  const WsLayout lay = ws_layout(a.num_seqs, a.num_q_heads, wph, grid);
+  uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+
+  decode_plan_kernel<<<1, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len, grid,
+                                             ws, a.err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  SplitParams sp;
+  sp.out = static_cast<__nv_bfloat16 *>(a.out);
+  sp.q = static_cast<const __nv_bfloat16 *>(a.q);
+  sp.k_cache = static_cast<const uint8_t *>(a.k_cache);
+  sp.v_cache = static_cast<const uint8_t *>(a.v_cache);
+  sp.block_tables = a.block_tables;
+  sp.max_blocks_per_seq = a.max_blocks_per_seq;
+  sp.num_seqs = a.num_seqs;
+  sp.num_q_heads = a.num_q_heads;
+  sp.num_kv_heads = a.num_kv_heads;
+  sp.block_size = a.block_size;
+  sp.num_blocks = a.num_blocks;
+  sp.qscale = a.scale * kLog2e;
+  sp.ws = ws;
+  sp.ml = reinterpret_cast<float2 *>(ws + lay.ml);
+  sp.po = reinterpret_cast<float *>(ws + lay.o);
+  sp.err = a.err;
+  const size_t smem = split_smem_bytes(group);
+  switch (group) {
+    case 1: decode_split_kernel<1><<<grid, kThreads, smem, stream>>>(sp); break;
+    case 2: decode_split_kernel<2><<<grid, kThreads, smem, stream>>>(sp); break;
+    case 4: decode_split_kernel<4><<<grid, kThreads, smem, stream>>>(sp); break;
+    default: decode_split_kernel<8><<<grid, kThreads, smem, stream>>>(sp); break;
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  CombineParams cp;
+  cp.out = sp.out;
+  cp.ws = ws;
+  cp.ml = sp.ml;
+  cp.po = sp.po;
+  cp.num_seqs = a.num_seqs;
+  cp.num_q_heads = a.num_q_heads;
+  cp.wph = wph;
+  cp.grid = grid;
+  decode_combine_kernel<<<a.num_seqs, 128, 0, stream>>>(cp);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

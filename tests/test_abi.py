@@ -1,0 +1,71 @@
+"""The C-ABI library builds, loads without a GPU, and exports every entry point
+that include/pkv.h declares (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_86_gb300 as pkv
+from paged_kv_cache_86_gb300 import _lib
+from paged_kv_cache_86_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return _lib.load()
+
+
+def test_header_declares_the_three_operations():
+    names = declared_functions()
+    for n in ("pkv_store_kvcache", "pkv_paged_decode", "pkv_paged_prefill"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(_lib.EXPORTED) <= set(declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    assert lib.pkv_status_string(0) == b"ok"
+    for code in range(-6, 0):
+        assert lib.pkv_status_string(code) != b"unknown status"
+    assert pkv.version() >= 100
+
+
+def test_host_validation_needs_no_gpu(lib):
+    # Argument checks run before any CUDA call, so they answer on a CPU-only host.
+    vp, null = ctypes.c_void_p, ctypes.c_void_p(0)
+    assert lib.pkv_store_kvcache(null, null, null, null, null, 1, 8, 128, 16, 4, 1024, 1024,
+                                 7, null) == -3            # dtype
+    assert lib.pkv_store_kvcache(null, null, null, null, null, -1, 8, 128, 16, 4, 1024, 1024,
+                                 0, null) == -1            # negative token count
+    assert lib.pkv_store_kvcache(null, null, null, null, null, 0, 8, 128, 16, 4, 1024, 1024,
+                                 0, null) == 0             # nothing to do
+    assert lib.pkv_store_kvcache(null, null, null, null, null, 3, 8, 128, 16, 4, 1024, 1024,
+                                 0, null) == -1            # null pointers
+    assert lib.pkv_store_kvcache(vp(16), vp(16), vp(16), vp(16), vp(16), 3, 1, 12, 16, 4, 12, 12,
+                                 0, null) == -2            # row not a multiple of 8 elements
+    assert lib.pkv_store_kvcache(vp(18), vp(16), vp(16), vp(16), vp(16), 3, 8, 128, 16, 4, 1024,
+                                 1024, 0, null) == -1      # misaligned key
+    assert lib.pkv_paged_decode(null, null, null, null, null, 4, null, 2, 64, 8, 2, 64, 16, 8,
+                                 0.1, null, 0, 0, null) == -2   # head_dim 64
+    assert lib.pkv_paged_decode(null, null, null, null, null, 4, null, 2, 65, 8, 2, 128, 16, 8,
+                                 0.1, null, 0, 0, null) == -1   # max_context_len > 4 * 16
+    assert lib.pkv_paged_decode(null, null, null, null, null, 4, null, 0, 64, 8, 2, 128, 16, 8,
+                                 0.1, null, 0, 0, null) == 0    # no sequences
+    assert lib.pkv_paged_decode(null, null, null, null, null, 4, null, 2, 64, 8, 2, 128, 16, 8,
+                                 float("nan"), null, 0, 0, null) == -1
+    assert lib.pkv_paged_prefill(null, null, null, null, null, null, 8, 8, null, 4, 1, 8, 8, 2,
+                                 128, 16, 8, 0.1, 1, null, 0, 1, null) == -3

@@ -1,0 +1,167 @@
+"""GPU parity of a decode step (store of the new tokens, then paged decode)
+against the oracle, within |gpu - oracle| <= 1e-2 * max(1, |oracle|)."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_86_gb300 as pkv
+from paged_kv_cache_86_gb300 import workloads as W
+from pkv_testutil import assert_close, decode_step_reference, device_meta
+
+pytestmark = pytest.mark.gpu
+
+
+def run_decode_step(w, t=None):
+    """GPU store + decode through the C ABI; returns (out, tensors before store)."""
+    t = t or {k: v.cuda() for k, v in w.tensors.items()}
+    m = device_meta(w)
+    pkv.store_kvcache(t["key"], t["value"], t["k_cache"], t["v_cache"], m["slot_mapping"])
+    out = pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], m["block_tables"],
+                           m["context_lens"], w.scale)
+    assert pkv.get_device_errors() == 0
+    return out
+
+
+def check(w, seq_ids=None, what=""):
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    seq_ids = np.arange(w.num_seqs) if seq_ids is None else np.asarray(seq_ids)
+    ref = decode_step_reference(w, seq_ids, t["k_cache"], t["v_cache"], t["q"], t["key"], t["value"])
+    out = run_decode_step(w, t)
+    return assert_close(out[torch.from_numpy(seq_ids).cuda()], ref, what or w.name)
+
+
+def test_decode_3seq_pages_example():
+    check(W.decode_3seq())
+
+
+def test_decode_64seq_reduced():
+    check(W.decode_64seq(num_seqs=12, max_len=1500))
+
+
+def test_decode_512seq_reduced():
+    check(W.decode_512seq(num_seqs=40, hi=900))
+
+
+def test_decode_longtail_reduced():
+    check(W.decode_longtail(num_long=2, long_len=6000, num_short=30, short_len=200))
+
+
+@pytest.mark.parametrize("hkv", [1, 2, 4, 8])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_decode_head_configurations(hkv, group):
+    lens = [1, 2, 15, 16, 17, 63, 200, 777]
+    w = W.decode_workload(f"heads_{hkv}x{group}", lens, hkv * group, hkv, 16, seed=100 + hkv * 10 + group)
+    check(w)
+
+
+@pytest.mark.parametrize("bs", [1, 3, 8, 64, 256, 1024])
+def test_decode_block_sizes(bs):
+    w = W.decode_workload(f"bs{bs}", [5, 300, 1, 1024, 77], 32, 8, bs, seed=200 + bs)
+    check(w)
+
+
+def test_decode_one_long_sequence_splits_over_every_cta():
+    # one 60000-token context is cut into many ranges: exercises the combine pass
+    w = W.decode_workload("one_long", [60000], 32, 8, 16, seed=11)
+    check(w)
+
+
+def test_decode_many_tiny_sequences():
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1, 9, size=3000)
+    w = W.decode_workload("tiny_many", lens, 32, 8, 16, seed=12)
+    check(w, seq_ids=np.concatenate([np.arange(0, 3000, 97), [2999]]))
+
+
+def test_decode_zero_context_rows_are_zero():
+    w = W.decode_workload("with_empty", [0, 40, 0, 3, 0], 8, 2, 16, seed=13)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    ref = decode_step_reference(w, np.arange(5), t["k_cache"], t["v_cache"], t["q"], t["key"], t["value"])
+    out = run_decode_step(w, t)
+    for i in (0, 2, 4):
+        assert (out[i] == 0).all()
+    assert_close(out, ref, "with_empty")
+
+
+def test_decode_context_one_returns_stored_value():
+    w = W.decode_workload("ctx1", [1] * 37, 32, 8, 16, seed=14)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    out = run_decode_step(w, t)
+    g = 4
+    for i in range(37):
+        for h in range(32):
+            assert torch.equal(out[i, h], t["value"][i, h // g])
+
+
+def test_decode_repeat_calls_are_deterministic_and_reuse_workspace():
+    w = W.decode_512seq(num_seqs=64, hi=2000)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    m = device_meta(w)
+    pkv.store_kvcache(t["key"], t["value"], t["k_cache"], t["v_cache"], m["slot_mapping"])
+    ws = torch.empty(pkv.decode_workspace_size(w.num_seqs, 32, 8), dtype=torch.uint8, device="cuda")
+    a = pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], m["block_tables"], m["context_lens"],
+                         w.scale, workspace=ws)
+    b = pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], m["block_tables"], m["context_lens"],
+                         w.scale, workspace=ws)
+    assert torch.equal(a, b)
+
+
+def test_decode_flags_bad_block_id_and_length():
+    w = W.decode_workload("bad_meta", [40, 40], 8, 2, 16, seed=15)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    m = device_meta(w)
+    bt = m["block_tables"].clone()
+    bt[0, 1] = w.num_blocks + 3
+    pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], bt, m["context_lens"], w.scale)
+    assert pkv.get_device_errors() & pkv._lib.DEVERR_BLOCK_ID
+    lens = m["context_lens"].clone()
+    lens[1] = 10_000
+    pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], m["block_tables"], lens, w.scale,
+                     max_context_len=64)
+    assert pkv.get_device_errors() & pkv._lib.DEVERR_LENGTH
+
+
+def test_decode_rejects_small_workspace():
+    w = W.decode_workload("ws", [4, 4], 8, 2, 16, seed=16)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    m = device_meta(w)
+    with pytest.raises(pkv.PkvError):
+        pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], m["block_tables"], m["context_lens"],
+                         w.scale, workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
+
+
+# ---- full-size workloads, in the launch configuration the bench times, on sampled sequences
+
+def _sample(w, k, seed):
+    rng = np.random.default_rng(seed)
+    lens = w.context_lens
+    pick = {int(np.argmax(lens)), int(np.argmin(lens))}
+    pick |= set(rng.choice(w.num_seqs, size=min(k, w.num_seqs), replace=False).tolist())
+    return np.array(sorted(pick))
+
+
+def test_decode_64seq_full_size_sampled():
+    w = W.decode_64seq(fill="device")
+    check(w, _sample(w, 8, 1))
+
+
+def test_decode_512seq_full_size_sampled():
+    w = W.decode_512seq(fill="device")
+    check(w, _sample(w, 24, 2))
+
+
+def test_decode_longtail_full_size_sampled():
+    w = W.decode_longtail(fill="device")
+    longs = np.nonzero(w.context_lens == 32768)[0][:2]
+    check(w, np.unique(np.concatenate([longs, _sample(w, 10, 3)])))
+
+
+def test_decode_full_size_all_rows_within_convex_hull():
+    """Any size: each output coordinate is a convex combination of the V values
+    it attends to, so it is finite and no larger in magnitude than max |V|."""
+    w = W.decode_512seq(fill="device")
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    out = run_decode_step(w, t)
+    vmax = max(t["v_cache"].abs().max().item(), t["value"].abs().max().item())
+    assert torch.isfinite(out.float()).all()
+    assert out.float().abs().max().item() <= vmax * (1 + 1e-2)
