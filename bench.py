@@ -48,6 +48,10 @@ def parse():
     ap.add_argument("--workload", default="decode_512seq")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="smaller case of the same workload recipe (profiling captures)")
+    ap.add_argument("--quick", action="store_true",
+                    help="warm-up and timed steps only: no per-op, e2e, clocks or CPU legs")
     return ap.parse_args()
 
 
@@ -125,12 +129,17 @@ class ClockSampler:
 
 # -------------------------------------------------------------- workloads --
 
-def make_workload(name, seed_offset=0, fill="device"):
+def make_workload(name, seed_offset=0, fill="device", num_seqs=None):
+    import inspect
     from paged_kv_cache_86_gb300 import workloads as W
     fn = W.NAMED[name]
-    import inspect
-    seed = inspect.signature(fn).parameters["seed"].default + seed_offset
-    return fn(seed=seed, fill=fill)
+    params = inspect.signature(fn).parameters
+    kw = {"seed": params["seed"].default + seed_offset, "fill": fill}
+    if num_seqs is not None:
+        if "num_seqs" not in params:
+            raise SystemExit(f"--num-seqs is not supported for {name}")
+        kw["num_seqs"] = num_seqs
+    return fn(**kw)
 
 
 def decode_bytes(w) -> int:
@@ -181,8 +190,12 @@ def cpu_oracle_sample(w, target_s=15.0, max_seqs=None):
     token_of_seq = np.cumsum(w.context_lens > 0) - 1
     bs = w.block_size
     batch = 8
-    while elapsed < target_s and done_seqs < w.num_seqs and (max_seqs is None or done_seqs < max_seqs):
-        ids = np.sort(order[done_seqs:done_seqs + batch])
+    passes = 0
+    while elapsed < target_s and (max_seqs is None or done_seqs < max_seqs):
+        start = done_seqs % w.num_seqs
+        if start == 0 and done_seqs:
+            passes += 1
+        ids = np.sort(order[start:start + batch])
         rows = w.block_tables[ids]
         nblk = [-(-int(w.context_lens[i]) // bs) for i in ids]
         used = np.unique(np.concatenate([rows[j, :n] for j, n in enumerate(nblk)]))
@@ -208,8 +221,9 @@ def cpu_oracle_sample(w, target_s=15.0, max_seqs=None):
         done_tokens += int(lens.sum())
     value = done_seqs / elapsed if elapsed > 0 else None
     return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done_seqs} of {w.num_seqs} sequences ({done_tokens} cached tokens), "
-                      f"store + decode in fp64 C with OpenMP, {elapsed:.1f} s",
+            "sample": f"{done_seqs} sequences of the {w.num_seqs}-sequence batch in seeded random "
+                      f"order, cycling ({done_tokens} cached tokens), store + decode in fp64 C "
+                      f"with OpenMP, {elapsed:.1f} s",
             "seconds": elapsed}
 
 
@@ -222,7 +236,7 @@ def run_pkv(args, rank, world, device):
     from paged_kv_cache_86_gb300 import _lib
 
     torch.cuda.set_device(device)
-    w = make_workload(args.workload, seed_offset=rank, fill="device")
+    w = make_workload(args.workload, seed_offset=rank, fill="device", num_seqs=args.num_seqs)
     t = {k: v.to(device) for k, v in w.tensors.items()}
     bt = torch.from_numpy(w.block_tables).to(device)
     cl = torch.from_numpy(w.context_lens).to(device)
@@ -259,6 +273,10 @@ def run_pkv(args, rank, world, device):
         torch.cuda.synchronize()
         barrier()
         step_ms = e0.elapsed_time(e1) / args.steps
+        if args.quick:
+            return {"metric": METRIC, "value": world * w.num_seqs / (step_ms * 1e-3), "unit": UNIT,
+                    "n_gpus": world, "steps": args.steps, "ms_per_step": step_ms,
+                    "config": {"workload": w.name, "num_seqs": w.num_seqs}, "quick": True}
 
         # per-op durations over the same number of steps, events on the launching stream
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),

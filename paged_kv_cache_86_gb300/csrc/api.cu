@@ -173,6 +173,7 @@ pkv_status pkv_paged_prefill(void *out, const void *q, const void *k_cache, cons
   if (head_dim != 128) return PKV_ERR_SHAPE;
   if (int64_t(max_seqlen_k) > int64_t(max_blocks_per_seq) * block_size) return PKV_ERR_ARG;
   if (!pkv::prefill_supported(num_q_heads, num_kv_heads, block_size)) return PKV_ERR_SHAPE;
+  if (num_seqs > 65535 || num_q_heads > 65535) return PKV_ERR_ARG;  // grid y / z limits
   if (num_seqs == 0 || total_q == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_tables)
     return PKV_ERR_ARG;

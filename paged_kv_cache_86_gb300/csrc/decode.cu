@@ -32,7 +32,7 @@
 //               normalised and written as bf16 directly; a sequence cut by a
 //               range boundary leaves a partial (o/l, m, l) for each of its
 //               pieces.
-//   3. combine  one CTA per sequence merges the partials of cut sequences
+//   3. combine  one warp per (sequence, query head) merges the partials of cut sequences
 //               with the log-sum-exp rule  M = max m_s,
 //               o = sum_s l_s 2^(m_s - M) o_s / sum_s l_s 2^(m_s - M),
 //               and writes zero rows for empty sequences.
@@ -315,7 +315,7 @@ decode_split_kernel(const SplitParams p) {
 
   for (int k = 0;; ++k) {
     const int s = k % kStages;
-    if (!mbar_wait(smem_addr(&full_bar[s]), (k / kStages) & 1, abort_flag)) {
+    if (!__all_sync(kFull, mbar_wait(smem_addr(&full_bar[s]), (k / kStages) & 1, abort_flag))) {
       if (lane == 0) {
         *abort_flag = 1;
         raise_error(p.err, PKV_DEVERR_TIMEOUT);
@@ -518,53 +518,75 @@ struct CombineParams {
   int grid;
 };
 
-__global__ void __launch_bounds__(128) decode_combine_kernel(const CombineParams p) {
-  const int i = blockIdx.x;
+// One warp per (sequence, query head); lane l owns dims 4l .. 4l+3. The
+// partial records of the sequence are enumerated in order; lanes first load
+// (m, l) of records lane, lane+32, ... so every load of a pass is independent.
+__device__ __forceinline__ int combine_record(const CombineParams &p, int i, int c0, int range,
+                                              int b_first, bool complete, int k) {
+  if (complete) return 2 * p.grid * p.wph + i * p.wph + k;
+  const int b = b_first + k / p.wph;
+  const int slot = (b == b_first && c0 > b * range) ? 2 * b + 1 : 2 * b;
+  return slot * p.wph + k % p.wph;
+}
+
+constexpr int kCombineWarps = 8;
+
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const CombineParams p) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (gw >= p.num_seqs * p.num_q_heads) return;
+  const int i = gw / p.num_q_heads;
+  const int qh = gw - i * p.num_q_heads;
   const Header hdr = *reinterpret_cast<const Header *>(p.ws);
   const int *cu = reinterpret_cast<const int *>(p.ws + 256);
   const int c0 = cu[i], c1 = cu[i + 1];
-  __nv_bfloat16 *orow = p.out + static_cast<size_t>(i) * p.num_q_heads * kHeadDim;
-  const int items = p.num_q_heads * (kHeadDim / 4);
+  uint2 *orow = reinterpret_cast<uint2 *>(p.out + (static_cast<size_t>(i) * p.num_q_heads + qh) * kHeadDim);
   if (c1 == c0) {  // empty context: zero row
-    for (int x = threadIdx.x; x < items; x += blockDim.x)
-      reinterpret_cast<uint2 *>(orow)[x] = make_uint2(0u, 0u);
+    orow[lane] = make_uint2(0u, 0u);
     return;
   }
   const int b_first = c0 / hdr.range;
   const int b_last = (c1 - 1) / hdr.range;
-  if (p.wph == 1 && b_first == b_last) return;  // written by the split kernel
-  for (int x = threadIdx.x; x < items; x += blockDim.x) {
-    const int qh = x / (kHeadDim / 4);
-    const int d4 = x % (kHeadDim / 4);
-    float m_max = -INFINITY;
-    for (int b = b_first; b <= b_last; ++b) {
-      const int base = b_first == b_last ? 2 * p.grid * p.wph + i * p.wph
-                                         : ((b == b_first && c0 > b * hdr.range) ? 2 * b + 1 : 2 * b) * p.wph;
-      for (int w = 0; w < p.wph; ++w)
-        m_max = fmaxf(m_max, p.ml[static_cast<size_t>(base + w) * p.num_q_heads + qh].x);
-    }
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    float l_tot = 0.f;
-    if (m_max != -INFINITY) {
-      for (int b = b_first; b <= b_last; ++b) {
-        const int base = b_first == b_last ? 2 * p.grid * p.wph + i * p.wph
-                                           : ((b == b_first && c0 > b * hdr.range) ? 2 * b + 1 : 2 * b) * p.wph;
-        for (int w = 0; w < p.wph; ++w) {
-          const size_t rec = static_cast<size_t>(base + w) * p.num_q_heads + qh;
-          const float2 ml = p.ml[rec];
-          const float wgt = ml.y * fast_exp2(ml.x - m_max);
-          const float4 v = reinterpret_cast<const float4 *>(p.po + rec * kHeadDim)[d4];
-          o.x += wgt * v.x; o.y += wgt * v.y; o.z += wgt * v.z; o.w += wgt * v.w;
-          l_tot += wgt;
-        }
+  const bool complete = b_first == b_last;
+  if (p.wph == 1 && complete) return;  // written by the split kernel
+  const int n = complete ? p.wph : (b_last - b_first + 1) * p.wph;
+
+  float m_max = -INFINITY;
+  for (int k = lane; k < n; k += 32) {
+    const int rec = combine_record(p, i, c0, hdr.range, b_first, complete, k);
+    m_max = fmaxf(m_max, p.ml[static_cast<size_t>(rec) * p.num_q_heads + qh].x);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) m_max = fmaxf(m_max, __shfl_xor_sync(kFull, m_max, off));
+
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l_tot = 0.f;
+  if (m_max != -INFINITY) {
+    for (int base = 0; base < n; base += 32) {
+      float wk = 0.f;
+      int rec_k = 0;
+      if (base + lane < n) {
+        rec_k = combine_record(p, i, c0, hdr.range, b_first, complete, base + lane);
+        const float2 ml = p.ml[static_cast<size_t>(rec_k) * p.num_q_heads + qh];
+        wk = ml.y * fast_exp2(ml.x - m_max);
+      }
+      const int cnt = min(32, n - base);
+#pragma unroll 4
+      for (int k = 0; k < cnt; ++k) {
+        const float wgt = __shfl_sync(kFull, wk, k);
+        const int rec = __shfl_sync(kFull, rec_k, k);
+        const float4 v = reinterpret_cast<const float4 *>(
+            p.po + (static_cast<size_t>(rec) * p.num_q_heads + qh) * kHeadDim)[lane];
+        o.x += wgt * v.x; o.y += wgt * v.y; o.z += wgt * v.z; o.w += wgt * v.w;
+        l_tot += wgt;
       }
     }
-    const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-    uint2 packed;
-    packed.x = float2_to_bf16x2(o.x * inv, o.y * inv);
-    packed.y = float2_to_bf16x2(o.z * inv, o.w * inv);
-    reinterpret_cast<uint2 *>(orow)[x] = packed;
   }
+  const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+  uint2 packed;
+  packed.x = float2_to_bf16x2(o.x * inv, o.y * inv);
+  packed.y = float2_to_bf16x2(o.z * inv, o.w * inv);
+  orow[lane] = packed;
 }
 
 size_t split_smem_bytes(int group) {
@@ -660,7 +682,9 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, int grid, cudaStream_t stre
   cp.num_q_heads = a.num_q_heads;
   cp.wph = wph;
   cp.grid = grid;
-  decode_combine_kernel<<<a.num_seqs, 128, 0, stream>>>(cp);
+  const int warps = a.num_seqs * a.num_q_heads;
+  decode_combine_kernel<<<(warps + kCombineWarps - 1) / kCombineWarps, kCombineWarps * 32, 0,
+                          stream>>>(cp);
   return cudaGetLastError();
 }
 

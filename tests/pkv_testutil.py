@@ -83,3 +83,15 @@ def assert_close(gpu: torch.Tensor, ref: np.ndarray, what: str = ""):
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements beyond tolerance; "
                              f"max err {err.max():.3e}; first at {idx.tolist()}")
     return float(err.max())
+
+
+def prefill_step_reference(w: Workload, k_cache, v_cache, q, key, value, row_mask=None):
+    """Oracle store of the chunk tokens, then oracle prefill (selected rows).
+
+    k_cache/v_cache are the caches before the step's store. Returns float64
+    [total_q, Hq, D] (NaN in rows not selected)."""
+    assert w.kind == "prefill"
+    kc, vc = bf16_to_u16(k_cache).copy(), bf16_to_u16(v_cache).copy()
+    oracle.store_kvcache(bf16_to_u16(key), bf16_to_u16(value), kc, vc, w.slot_mapping, w.block_size)
+    return oracle.paged_prefill(bf16_to_u16(q), kc, vc, w.cu_seqlens_q, w.cu_seqlens_k,
+                                w.block_tables, w.scale, causal=True, row_mask=row_mask)

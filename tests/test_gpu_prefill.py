@@ -1,0 +1,97 @@
+"""GPU parity of a chunked-prefill step (store of the chunk, then paged varlen
+causal prefill on tcgen05) against the oracle, within
+|gpu - oracle| <= 1e-2 * max(1, |oracle|)."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_86_gb300 as pkv
+from paged_kv_cache_86_gb300 import workloads as W
+from pkv_testutil import assert_close, device_meta, prefill_step_reference
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill_step(w, t, causal=True):
+    m = device_meta(w)
+    pkv.store_kvcache(t["key"], t["value"], t["k_cache"], t["v_cache"], m["slot_mapping"])
+    out = pkv.paged_prefill(t["q"], t["k_cache"], t["v_cache"], m["cu_seqlens_q"], m["cu_seqlens_k"],
+                            m["block_tables"], w.scale, max_seqlen_q=int(w.q_lens.max()),
+                            max_seqlen_k=int(w.context_lens.max()), causal=causal)
+    assert pkv.get_device_errors() == 0
+    return out
+
+
+def check(w, rows=None, what=""):
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    mask = None
+    if rows is not None:
+        mask = np.zeros(w.num_q_rows, np.uint8)
+        mask[rows] = 1
+    ref = prefill_step_reference(w, t["k_cache"], t["v_cache"], t["q"], t["key"], t["value"], mask)
+    out = run_prefill_step(w, t)
+    sel = np.arange(w.num_q_rows) if rows is None else np.asarray(rows)
+    return assert_close(out[torch.from_numpy(sel).cuda()], ref[sel], what or w.name)
+
+
+def test_prefill_small_chunks_ragged_tiles():
+    check(W.prefill_chunks(num_seqs=4, q_len=200, max_prefix=300))
+
+
+def test_prefill_single_tile_no_prefix():
+    check(W.prefill_workload("p_one", [128], [0], 32, 8, 16, seed=1))
+
+
+@pytest.mark.parametrize("q_lens,prefixes", [
+    ([1, 5, 128, 129, 300], [0, 17, 64, 3, 250]),
+    ([64, 64], [1000, 1]),
+    ([257], [0]),
+])
+def test_prefill_varlen(q_lens, prefixes):
+    check(W.prefill_workload("p_varlen", q_lens, prefixes, 32, 8, 16, seed=sum(q_lens)))
+
+
+@pytest.mark.parametrize("bs", [8, 16, 24, 32, 128, 256])
+def test_prefill_block_sizes(bs):
+    check(W.prefill_workload(f"p_bs{bs}", [130, 77], [300, 45], 16, 8, bs, seed=300 + bs))
+
+
+@pytest.mark.parametrize("hkv,group", [(8, 1), (4, 2), (8, 4), (2, 8), (1, 4)])
+def test_prefill_head_groups(hkv, group):
+    check(W.prefill_workload(f"p_h{hkv}g{group}", [140, 33], [200, 7], hkv * group, hkv, 16,
+                             seed=400 + hkv * 10 + group))
+
+
+def test_prefill_noncausal_matches_oracle():
+    from oracle import attention as oracle
+    from paged_kv_cache_86_gb300.workloads import bf16_to_u16
+    w = W.prefill_workload("p_noncausal", [100, 60], [40, 0], 16, 8, 16, seed=9)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    kc, vc = bf16_to_u16(t["k_cache"]).copy(), bf16_to_u16(t["v_cache"]).copy()
+    oracle.store_kvcache(bf16_to_u16(t["key"]), bf16_to_u16(t["value"]), kc, vc, w.slot_mapping,
+                         w.block_size)
+    ref = oracle.paged_prefill(bf16_to_u16(t["q"]), kc, vc, w.cu_seqlens_q, w.cu_seqlens_k,
+                               w.block_tables, w.scale, causal=False)
+    out = run_prefill_step(w, t, causal=False)
+    assert_close(out, ref, "noncausal")
+
+
+def test_prefill_last_row_matches_decode():
+    w = W.prefill_chunks(num_seqs=6, q_len=150, max_prefix=700)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    out = run_prefill_step(w, t)
+    m = device_meta(w)
+    last = torch.from_numpy((w.cu_seqlens_q[1:] - 1).astype(np.int64)).cuda()
+    dec = pkv.paged_decode(t["q"][last].contiguous(), t["k_cache"], t["v_cache"], m["block_tables"],
+                           m["context_lens"], w.scale)
+    diff = (out[last].float() - dec.float()).abs()
+    assert diff.max().item() <= 2e-2 * max(1.0, dec.float().abs().max().item())
+
+
+def test_prefill_full_size_sampled_rows():
+    w = W.prefill_chunks()
+    assert w.num_q_rows == 16384
+    rng = np.random.default_rng(5)
+    rows = set(rng.choice(w.num_q_rows, size=96, replace=False).tolist())
+    rows |= set(w.cu_seqlens_q[:-1].tolist()) | set((w.cu_seqlens_q[1:] - 1).tolist())
+    check(w, rows=sorted(rows))
