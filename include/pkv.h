@@ -133,6 +133,36 @@ pkv_status pkv_paged_decode(void *out, const void *q,
                             void *workspace, size_t workspace_bytes,
                             pkv_dtype dtype, void *stream);
 
+/* ------------------------------------------------- decode, no allocation --
+ * pkv_paged_decode_static_ws: the same computation, arguments and errors as
+ * pkv_paged_decode, for callers that cannot give the library any device memory
+ * of its own -- e.g. a plug-in inside a framework whose allocator owns the
+ * device, or a runtime that only hands over its input and output buffers. The
+ * call allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine): its scratch space is one fixed 16 MiB device array compiled into
+ * the library, which every GPU that loads the library keeps until the process
+ * exits. None of the source pages has a counterpart of this call; it exists
+ * only for such callers.
+ *   Limit: a batch whose pkv_decode_workspace_size(num_seqs, num_q_heads,
+ *   num_kv_heads, head_dim) exceeds 16 MiB (16777216 bytes) is rejected with
+ *   PKV_ERR_WORKSPACE before anything is launched.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current and caches it; make that
+ *   first call before any stream capture.
+ *   Sharing: all calls share the one array and it keeps the last call's
+ *   contents (nothing in it needs to start at zero). Calls whose kernels may
+ *   overlap on the GPU (different streams without ordering) race on it; order
+ *   them on one stream.
+ */
+pkv_status pkv_paged_decode_static_ws(void *out, const void *q,
+                                      const void *k_cache, const void *v_cache,
+                                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t *context_lens, int32_t num_seqs,
+                                      int32_t max_context_len,
+                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int32_t num_blocks, float scale,
+                                      pkv_dtype dtype, void *stream);
+
 /* --------------------------------------------------------------- prefill --
  * Sequence i owns query rows cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1 (q_len
  * rows) and keys 0 .. k_len-1 with k_len = cu_seqlens_k[i+1] - cu_seqlens_k[i],
