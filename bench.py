@@ -52,6 +52,8 @@ def parse():
                     help="smaller case of the same workload recipe (profiling captures)")
     ap.add_argument("--quick", action="store_true",
                     help="warm-up and timed steps only: no per-op, e2e, clocks or CPU legs")
+    ap.add_argument("--only-prefill", action="store_true",
+                    help="time only the chunked-prefill row (store + prefill), for profiling")
     return ap.parse_args()
 
 
@@ -365,9 +367,74 @@ def run_pkv(args, rank, world, device):
         "gpu_launches": args.steps * 4,
         "clocks": clocks.summary(),
     }
+    result["prefill_row"] = measure_prefill(args, device, steps=max(5, min(args.steps, 20)))
+    result["gpu_launches_prefill_row"] = 2 * max(5, min(args.steps, 20))
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_oracle_sample(w)
     return result
+
+
+def prefill_flops(w) -> int:
+    """Causal-region FLOPs of one prefill launch: 2 contractions x 2 flops per
+    multiply-add x D x Hq x (keys each query row sees)."""
+    q_lens = np.diff(w.cu_seqlens_q).astype(np.int64)
+    k_lens = np.diff(w.cu_seqlens_k).astype(np.int64)
+    vis = sum(int(((k - q) + np.arange(1, q + 1)).sum()) for q, k in zip(q_lens, k_lens))
+    return 4 * w.head_dim * w.num_q_heads * vis
+
+
+def measure_prefill(args, device, steps):
+    """The chunked-prefill row: store of 16384 chunk tokens, then causal paged
+    prefill of 32 chunks of 512 over cached prefixes, each timed with CUDA events."""
+    import torch
+    import paged_kv_cache_86_gb300 as pkv
+    w = make_workload("prefill_chunks", fill="device")
+    t = {k: v.to(device) for k, v in w.tensors.items()}
+    bt = torch.from_numpy(w.block_tables).to(device)
+    sm = torch.from_numpy(w.slot_mapping).to(device)
+    cq = torch.from_numpy(w.cu_seqlens_q).to(device)
+    ck = torch.from_numpy(w.cu_seqlens_k).to(device)
+    out = torch.empty_like(t["q"])
+    mq, mk = int(w.q_lens.max()), int(w.context_lens.max())
+    stream = torch.cuda.current_stream(device)
+
+    def store():
+        pkv.store_kvcache(t["key"], t["value"], t["k_cache"], t["v_cache"], sm)
+
+    def prefill():
+        pkv.paged_prefill(t["q"], t["k_cache"], t["v_cache"], cq, ck, bt, w.scale, mq, mk, out=out)
+
+    for _ in range(3):
+        store()
+        prefill()
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # > L2 between launches
+    res = {}
+    for name, fn in (("store", store), ("prefill", prefill)):
+        times = []
+        for _ in range(steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        res[name] = statistics.mean(times)
+    if pkv.get_device_errors() != 0:
+        raise RuntimeError("device-side range check fired in the prefill measurement")
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    tpeak = float(peaks.get("bf16_tflops", 1900.0))
+    hpeak, _ = measured_peaks()
+    fl = prefill_flops(w)
+    sb = store_bytes(w)
+    return {"workload": w.name, "l2": "256 MiB buffer written between launches",
+            "store_ms": res["store"], "store_gbs": sb / (res["store"] * 1e-3) / 1e9,
+            "store_frac_of_hbm": sb / (res["store"] * 1e-3) / 1e9 / hpeak,
+            "prefill_ms": res["prefill"], "prefill_tflops": fl / (res["prefill"] * 1e-3) / 1e12,
+            "prefill_frac_of_bf16": fl / (res["prefill"] * 1e-3) / 1e12 / tpeak,
+            "prefill_flops": fl, "peak_bf16_tflops": tpeak, "peak_source": "measured bf16_tflops (burst)"}
 
 
 def run_reference(args, rank):
@@ -417,7 +484,11 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    res = run_pkv(args, rank, world, device)
+    if args.only_prefill:
+        torch.cuda.set_device(device)
+        res = {"prefill_row": measure_prefill(args, device, steps=max(1, args.steps))}
+    else:
+        res = run_pkv(args, rank, world, device)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -34,7 +34,8 @@ sequence's last block and to a row length rounded up to 32 entries.
 Values: metadata comes from numpy's default_rng(seed). bf16 values are
 fp32 N(0, 1) draws rounded to nearest even, from torch's generator seeded
 with seed + a per-tensor offset, on the host ("host" fill) or on the GPU
-("device" fill, for pools too large to draw on the host quickly).
+("device" fill, for pools too large to draw on the host quickly); "none"
+draws metadata only.
 """
 from __future__ import annotations
 
@@ -157,6 +158,9 @@ def _slots(tables, positions_per_seq, bs):
 
 
 def _fill_values(w: Workload, fill: str, device: str | None):
+    if fill == "none":  # metadata only
+        w.tensors = {}
+        return w
     dev = "cpu" if fill == "host" else (device or "cuda")
     hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
     shapes = {
