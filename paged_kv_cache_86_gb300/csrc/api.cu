@@ -89,11 +89,11 @@ pkv_status pkv_store_kvcache(const void *key, const void *value, void *k_cache, 
 
 size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim) {
-  if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim != 128) return 0;
+  if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim != 128 ||
+      num_q_heads % num_kv_heads != 0)
+    return 0;
   cudaError_t e;
-  const int grid = pkv::decode_grid(num_q_heads, num_kv_heads, &e);
-  if (grid <= 0) return 0;
-  return pkv::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, grid);
+  return pkv::decode_workspace_upper_bound(num_seqs, num_q_heads, num_kv_heads, &e);
 }
 
 pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -109,7 +109,7 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
     return PKV_ERR_ARG;
   if (head_dim != 128) return PKV_ERR_SHAPE;
   if (int64_t(max_context_len) > int64_t(max_blocks_per_seq) * block_size) return PKV_ERR_ARG;
-  if (int64_t(num_seqs) * max_context_len >= (int64_t(1) << 31)) return PKV_ERR_ARG;
+  if (int64_t(num_seqs) * max_context_len * num_kv_heads >= (int64_t(1) << 31)) return PKV_ERR_ARG;
   if (num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !context_lens ||
       (!block_tables && max_blocks_per_seq > 0))
@@ -117,11 +117,12 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_ARG;
   cudaError_t e;
-  const int grid = pkv::decode_grid(num_q_heads, num_kv_heads, &e);
-  if (e != cudaSuccess) return PKV_ERR_CUDA;
-  if (grid <= 0) return PKV_ERR_SHAPE;
+  pkv::DecodePlan plan;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_SHAPE;
+  if (!pkv::choose_decode_plan(num_q_heads, num_kv_heads, block_size, &plan, &e))
+    return e != cudaSuccess ? PKV_ERR_CUDA : PKV_ERR_SHAPE;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
-      workspace_bytes < pkv::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, grid))
+      workspace_bytes < pkv::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, plan))
     return PKV_ERR_WORKSPACE;
   uint32_t *err = pkv::device_error_word(&e);
   if (!err) return PKV_ERR_CUDA;
@@ -143,7 +144,7 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.err = err;
-  return from_cuda(pkv::launch_paged_decode(a, grid, static_cast<cudaStream_t>(stream)));
+  return from_cuda(pkv::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)));
 }
 
 size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,

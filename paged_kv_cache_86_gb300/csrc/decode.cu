@@ -94,9 +94,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // ------------------------------------------------------------------ plan --
 
+// units_per_token: 1 when a CTA range covers tokens of all KV heads (split
+// kernel), num_kv_heads when it covers (KV head, token) pairs (tcgen05 kernel).
 __global__ void __launch_bounds__(1024)
 decode_plan_kernel(const int32_t *__restrict__ context_lens, int num_seqs, int max_context_len,
-                   int grid, uint8_t *ws, uint32_t *err) {
+                   int grid, int units_per_token, int min_range, uint8_t *ws, uint32_t *err) {
   __shared__ int warp_sums[32];
   __shared__ int base;
   int *cu = reinterpret_cast<int *>(ws + 256);
@@ -143,10 +145,11 @@ decode_plan_kernel(const int32_t *__restrict__ context_lens, int num_seqs, int m
   if (threadIdx.x == 0) {
     Header *h = reinterpret_cast<Header *>(ws);
     const int total = base;
-    int range = (total + grid - 1) / grid;
+    const long long units = static_cast<long long>(total) * units_per_token;
+    long long range = (units + grid - 1) / grid;
     range = (range + 15) / 16 * 16;
     h->total = total;
-    h->range = range < kMinRange ? kMinRange : range;
+    h->range = static_cast<int>(range < min_range ? min_range : range);
   }
 }
 
@@ -516,17 +519,31 @@ struct CombineParams {
   int num_q_heads;
   int wph;
   int grid;
+  int tc;      // records of the tcgen05 kernel: one row per (slot, query head of the group)
+  int group;
 };
 
 // One warp per (sequence, query head); lane l owns dims 4l .. 4l+3. The
 // partial records of the sequence are enumerated in order; lanes first load
 // (m, l) of records lane, lane+32, ... so every load of a pass is independent.
-__device__ __forceinline__ int combine_record(const CombineParams &p, int i, int c0, int range,
-                                              int b_first, bool complete, int k) {
-  if (complete) return 2 * p.grid * p.wph + i * p.wph + k;
-  const int b = b_first + k / p.wph;
-  const int slot = (b == b_first && c0 > b * range) ? 2 * b + 1 : 2 * b;
-  return slot * p.wph + k % p.wph;
+// Returns the record row: ml[row], po[row * 128 ..].
+__device__ __forceinline__ long long combine_row(const CombineParams &p, int i, int qh,
+                                                 long long start, int range, long long b_first,
+                                                 bool complete, int k) {
+  if (p.tc) {
+    const long long b = b_first + k;
+    const long long slot = (b == b_first && start > b * range) ? 2 * b + 1 : 2 * b;
+    return slot * p.group + qh % p.group;
+  }
+  long long rec;
+  if (complete) {
+    rec = 2LL * p.grid * p.wph + static_cast<long long>(i) * p.wph + k;
+  } else {
+    const long long b = b_first + k / p.wph;
+    const long long slot = (b == b_first && start > b * range) ? 2 * b + 1 : 2 * b;
+    rec = slot * p.wph + k % p.wph;
+  }
+  return rec * p.num_q_heads + qh;
 }
 
 constexpr int kCombineWarps = 8;
@@ -545,16 +562,19 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     orow[lane] = make_uint2(0u, 0u);
     return;
   }
-  const int b_first = c0 / hdr.range;
-  const int b_last = (c1 - 1) / hdr.range;
+  // position of this (head, sequence) in the flat space the CTA ranges cut
+  const long long start = p.tc ? static_cast<long long>(qh / p.group) * hdr.total + c0 : c0;
+  const long long b_first = start / hdr.range;
+  const long long b_last = (start + (c1 - c0) - 1) / hdr.range;
   const bool complete = b_first == b_last;
-  if (p.wph == 1 && complete) return;  // written by the split kernel
-  const int n = complete ? p.wph : (b_last - b_first + 1) * p.wph;
+  if ((p.tc || p.wph == 1) && complete) return;  // written directly by the attention kernel
+  const int n = p.tc ? static_cast<int>(b_last - b_first + 1)
+                     : (complete ? p.wph : static_cast<int>(b_last - b_first + 1) * p.wph);
 
   float m_max = -INFINITY;
   for (int k = lane; k < n; k += 32) {
-    const int rec = combine_record(p, i, c0, hdr.range, b_first, complete, k);
-    m_max = fmaxf(m_max, p.ml[static_cast<size_t>(rec) * p.num_q_heads + qh].x);
+    const long long row = combine_row(p, i, qh, start, hdr.range, b_first, complete, k);
+    m_max = fmaxf(m_max, p.ml[row].x);
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) m_max = fmaxf(m_max, __shfl_xor_sync(kFull, m_max, off));
@@ -564,19 +584,18 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   if (m_max != -INFINITY) {
     for (int base = 0; base < n; base += 32) {
       float wk = 0.f;
-      int rec_k = 0;
+      long long row_k = 0;
       if (base + lane < n) {
-        rec_k = combine_record(p, i, c0, hdr.range, b_first, complete, base + lane);
-        const float2 ml = p.ml[static_cast<size_t>(rec_k) * p.num_q_heads + qh];
+        row_k = combine_row(p, i, qh, start, hdr.range, b_first, complete, base + lane);
+        const float2 ml = p.ml[row_k];
         wk = ml.y * fast_exp2(ml.x - m_max);
       }
       const int cnt = min(32, n - base);
 #pragma unroll 4
       for (int k = 0; k < cnt; ++k) {
         const float wgt = __shfl_sync(kFull, wk, k);
-        const int rec = __shfl_sync(kFull, rec_k, k);
-        const float4 v = reinterpret_cast<const float4 *>(
-            p.po + (static_cast<size_t>(rec) * p.num_q_heads + qh) * kHeadDim)[lane];
+        const long long row = __shfl_sync(kFull, row_k, k);
+        const float4 v = reinterpret_cast<const float4 *>(p.po + row * kHeadDim)[lane];
         o.x += wgt * v.x; o.y += wgt * v.y; o.z += wgt * v.z; o.w += wgt * v.w;
         l_tot += wgt;
       }
@@ -614,7 +633,7 @@ bool supported_heads(int num_q_heads, int num_kv_heads) {
 
 }  // namespace
 
-int decode_grid(int num_q_heads, int num_kv_heads, cudaError_t *status) {
+int split_grid(int num_q_heads, int num_kv_heads, cudaError_t *status) {
   *status = cudaSuccess;
   if (!supported_heads(num_q_heads, num_kv_heads)) return 0;
   int dev = 0;
@@ -630,58 +649,129 @@ int decode_grid(int num_q_heads, int num_kv_heads, cudaError_t *status) {
   return per_sm * sm_count(dev);
 }
 
-size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int grid) {
-  const int wph = kConsumerWarps / num_kv_heads;
-  return ws_layout(num_seqs, num_q_heads, wph, grid).total;
+size_t tc_workspace(int num_seqs, int group, int grid) {
+  const size_t rows = size_t(2) * grid * group;
+  const size_t ml = align256(256 + sizeof(int) * (size_t(num_seqs) + 1));
+  const size_t o = align256(ml + sizeof(float2) * rows);
+  return align256(o + sizeof(float) * rows * kHeadDim);
 }
 
-cudaError_t launch_paged_decode(const DecodeArgs &a, int grid, cudaStream_t stream) {
+bool choose_decode_plan(int num_q_heads, int num_kv_heads, int block_size, DecodePlan *plan,
+                        cudaError_t *status) {
+  *status = cudaSuccess;
+  if (decode_tcg_supported(num_q_heads, num_kv_heads, block_size)) {
+    plan->kind = 3;
+    plan->tc = false;
+    plan->grid = decode_tc_grid();
+    return plan->grid > 0;
+  }
+  if (decode_tc_supported(num_q_heads, num_kv_heads, block_size)) {
+    plan->kind = 2;
+    plan->tc = true;
+    plan->grid = decode_tc_grid();
+    return plan->grid > 0;
+  }
+  plan->kind = 1;
+  plan->tc = false;
+  plan->grid = split_grid(num_q_heads, num_kv_heads, status);
+  return plan->grid > 0;
+}
+
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                              const DecodePlan &plan) {
+  if (plan.kind == 2) return tc_workspace(num_seqs, num_q_heads / num_kv_heads, plan.grid);
+  const int wph = plan.kind == 1 ? kConsumerWarps / num_kv_heads : 1;
+  return ws_layout(num_seqs, num_q_heads, wph, plan.grid).total;
+}
+
+size_t decode_workspace_upper_bound(int num_seqs, int num_q_heads, int num_kv_heads,
+                                    cudaError_t *status) {
+  size_t need = 0;
+  DecodePlan plan;
+  // the kernel depends on the block size: try one of each kind
+  for (int bs : {128, 8, 1}) {
+    if (choose_decode_plan(num_q_heads, num_kv_heads, bs, &plan, status)) {
+      const size_t s = decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, plan);
+      if (s > need) need = s;
+    }
+  }
+  *status = cudaSuccess;
+  return need;
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
+  const int grid = plan.grid;
   const int wph = kConsumerWarps / a.num_kv_heads;
   const int group = a.num_q_heads / a.num_kv_heads;
-  const WsLayout lay = ws_layout(a.num_seqs, a.num_q_heads, wph, grid);
   uint8_t *ws = static_cast<uint8_t *>(a.workspace);
-
-  decode_plan_kernel<<<1, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len, grid,
-                                             ws, a.err);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
-  SplitParams sp;
-  sp.out = static_cast<__nv_bfloat16 *>(a.out);
-  sp.q = static_cast<const __nv_bfloat16 *>(a.q);
-  sp.k_cache = static_cast<const uint8_t *>(a.k_cache);
-  sp.v_cache = static_cast<const uint8_t *>(a.v_cache);
-  sp.block_tables = a.block_tables;
-  sp.max_blocks_per_seq = a.max_blocks_per_seq;
-  sp.num_seqs = a.num_seqs;
-  sp.num_q_heads = a.num_q_heads;
-  sp.num_kv_heads = a.num_kv_heads;
-  sp.block_size = a.block_size;
-  sp.num_blocks = a.num_blocks;
-  sp.qscale = a.scale * kLog2e;
-  sp.ws = ws;
-  sp.ml = reinterpret_cast<float2 *>(ws + lay.ml);
-  sp.po = reinterpret_cast<float *>(ws + lay.o);
-  sp.err = a.err;
-  const size_t smem = split_smem_bytes(group);
-  switch (group) {
-    case 1: decode_split_kernel<1><<<grid, kThreads, smem, stream>>>(sp); break;
-    case 2: decode_split_kernel<2><<<grid, kThreads, smem, stream>>>(sp); break;
-    case 4: decode_split_kernel<4><<<grid, kThreads, smem, stream>>>(sp); break;
-    default: decode_split_kernel<8><<<grid, kThreads, smem, stream>>>(sp); break;
-  }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaError_t e;
 
   CombineParams cp;
-  cp.out = sp.out;
+  cp.out = static_cast<__nv_bfloat16 *>(a.out);
   cp.ws = ws;
-  cp.ml = sp.ml;
-  cp.po = sp.po;
   cp.num_seqs = a.num_seqs;
   cp.num_q_heads = a.num_q_heads;
   cp.wph = wph;
   cp.grid = grid;
+  cp.group = group;
+  cp.tc = plan.tc ? 1 : 0;
+
+  if (plan.kind == 3) {
+    const WsLayout lay = ws_layout(a.num_seqs, a.num_q_heads, 1, grid);
+    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len, grid,
+                                               1, 128, ws, a.err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cp.wph = 1;
+    cp.ml = reinterpret_cast<float2 *>(ws + lay.ml);
+    cp.po = reinterpret_cast<float *>(ws + lay.o);
+    if ((e = launch_decode_tcg(a, grid, reinterpret_cast<float2 *>(ws + lay.ml),
+                               reinterpret_cast<float *>(ws + lay.o), stream)) != cudaSuccess)
+      return e;
+  } else if (plan.kind == 2) {
+    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len, grid,
+                                               a.num_kv_heads, 128, ws, a.err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t ml = align256(256 + sizeof(int) * (size_t(a.num_seqs) + 1));
+    const size_t o = align256(ml + sizeof(float2) * size_t(2) * grid * group);
+    cp.ml = reinterpret_cast<float2 *>(ws + ml);
+    cp.po = reinterpret_cast<float *>(ws + o);
+    if ((e = launch_decode_tc(a, grid, reinterpret_cast<float2 *>(ws + ml),
+                              reinterpret_cast<float *>(ws + o), stream)) != cudaSuccess)
+      return e;
+  } else {
+    const WsLayout lay = ws_layout(a.num_seqs, a.num_q_heads, wph, grid);
+    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len, grid,
+                                               1, kMinRange, ws, a.err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    SplitParams sp;
+    sp.out = static_cast<__nv_bfloat16 *>(a.out);
+    sp.q = static_cast<const __nv_bfloat16 *>(a.q);
+    sp.k_cache = static_cast<const uint8_t *>(a.k_cache);
+    sp.v_cache = static_cast<const uint8_t *>(a.v_cache);
+    sp.block_tables = a.block_tables;
+    sp.max_blocks_per_seq = a.max_blocks_per_seq;
+    sp.num_seqs = a.num_seqs;
+    sp.num_q_heads = a.num_q_heads;
+    sp.num_kv_heads = a.num_kv_heads;
+    sp.block_size = a.block_size;
+    sp.num_blocks = a.num_blocks;
+    sp.qscale = a.scale * kLog2e;
+    sp.ws = ws;
+    sp.ml = reinterpret_cast<float2 *>(ws + lay.ml);
+    sp.po = reinterpret_cast<float *>(ws + lay.o);
+    sp.err = a.err;
+    cp.ml = sp.ml;
+    cp.po = sp.po;
+    const size_t smem = split_smem_bytes(group);
+    switch (group) {
+      case 1: decode_split_kernel<1><<<grid, kThreads, smem, stream>>>(sp); break;
+      case 2: decode_split_kernel<2><<<grid, kThreads, smem, stream>>>(sp); break;
+      case 4: decode_split_kernel<4><<<grid, kThreads, smem, stream>>>(sp); break;
+      default: decode_split_kernel<8><<<grid, kThreads, smem, stream>>>(sp); break;
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   const int warps = a.num_seqs * a.num_q_heads;
   decode_combine_kernel<<<(warps + kCombineWarps - 1) / kCombineWarps, kCombineWarps * 32, 0,
                           stream>>>(cp);

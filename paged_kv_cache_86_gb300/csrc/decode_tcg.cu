@@ -1,0 +1,700 @@
+// decode_tcg.cu -- paged decode attention on tcgen05, all KV heads of a block
+// per stage (sm_103a). This is the fast decode path for GQA shapes.
+//
+// Computes what decode.cu computes (one query per sequence over its
+// context_lens[i] tokens, read through block_tables; nano vllm代码详解 §2
+// context; 推理运行时 §分页 KV). Decode is HBM-bound (Mini-SGLang 源码解析（二）
+// §8.3), and on GB300 the bytes only move at full speed when each copy covers
+// whole token rows: in the [NB, bs, Hkv, D] cache a run of T tokens of one
+// block is T * Hkv * 256 contiguous bytes. So a stage here is T = 128 / Hkv
+// consecutive tokens of one block with ALL their KV heads: 128 rows, loaded by
+// one tiled TMA box per 64-dim half through a (dim, token, head) view of the
+// cache, which lands in shared memory ordered [head][token][dim] -- exactly the
+// 128-row K-major operand the tensor core wants.
+//
+//   S^T[128 rows x N] = K[128 rows x 128 d] . Q^T[N x 128 d]     (N = Hq padded to 16)
+//     row h*T + t is token t of KV head h; column n = h'*G + g is query head n.
+//     Only the columns of the row's own head (h' = h) are used; the others are
+//     spare tensor-core work, which costs nothing here.
+//   O^T[128 d x N] += V^T[128 d x 128 rows] . P^T[128 rows x N]
+//     P^T is block-diagonal: row h*T + t holds p only in the columns of head h,
+//     so each query head accumulates only the V rows of its own KV head.
+//
+// Per CTA (192 threads, one CTA per SM): warp 0 is the TMA producer (Q rows of a
+// sequence when a segment starts, then K and V boxes per stage, three stages of
+// 64 KB), warp 1 owns TMEM and issues the MMAs, warps 2-5 run the softmax with
+// one thread per row: the T rows of a KV head sit in one warp, so the per-head
+// stage maximum and the row sums are warp shuffles. The running maximum is
+// rescaled lazily (only when it grows by more than 2^8), and the rare rescale of
+// O^T is broadcast through shared memory with one barrier per stage. Rows of
+// tokens outside the segment are masked and their V rows zeroed, so unwritten
+// cache slots never reach the PV MMA.
+//
+// CTA b owns the flat token range [bW, (b+1)W) of the concatenated contexts
+// (all heads), exactly like the split kernel in decode.cu, and leaves the same
+// partial records (o/l, m, l) for sequences a range boundary cuts; decode.cu's
+// combine kernel merges them.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+#include "pkv_tc.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kRows = 128;            // MMA M: rows of a stage (T tokens x Hkv heads)
+constexpr int kHD = 128;
+constexpr int kRegion = 16384;        // 128 rows x 128 B (one 64-dim half)
+constexpr int kKVBytes = 2 * kRegion;
+constexpr int kThreads = 192;
+constexpr int kMaxN = 128;
+constexpr int kMaxG = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.f;
+
+enum : int { kFirst = 1, kLast = 2, kEnd = 4 };
+
+struct GDesc {
+  int seq, pa, p0, p1, flags, slot, qbuf, pad;
+};
+
+struct GParams {
+  __nv_bfloat16 *out;
+  const int32_t *block_tables;
+  int max_blocks_per_seq;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int n_cols;          // N: num_q_heads rounded up to 16
+  int tokens;          // T = 128 / num_kv_heads
+  int block_size;
+  int num_blocks;
+  int stages;
+  int tmem_cols;
+  float scale_log2;
+  const uint8_t *ws;
+  float2 *ml;
+  float *po;
+  uint32_t *err;
+};
+
+// shared-memory map, all offsets from a 1024-aligned base
+struct GLayout {
+  int k, v, q, p, alpha, lsum, msum, desc, bar, total;
+};
+
+__host__ __device__ inline GLayout g_layout(int stages, int n_cols) {
+  GLayout L;
+  const int small = n_cols * 128;         // one 64-dim half of Q^T / P^T (N rows x 128 B)
+  L.k = 0;
+  L.v = stages * kKVBytes;
+  L.q = 2 * stages * kKVBytes;            // two Q^T buffers (2 halves each)
+  L.p = L.q + 2 * 2 * small;              // P^T (2 halves over the 128 rows)
+  L.alpha = L.p + 2 * small;              // [2][kMaxN] rescale factors, [2] stage flags
+  L.lsum = L.alpha + (2 * kMaxN + 4) * 4; // [kMaxN] row sums
+  L.msum = L.lsum + kMaxN * 4;            // [kMaxN] maxima
+  L.desc = L.msum + kMaxN * 4;
+  L.bar = L.desc + 4 * 32;
+  L.total = L.bar + 16 * 8 + 16;
+  return L;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// C consecutive fp32 TMEM columns of this thread's lane (warp-collective), C in {1..32}.
+template <int C>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[C]) {
+  uint32_t r[C];
+  if constexpr (C == 1) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr));
+  } else if constexpr (C == 2) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+  } else if constexpr (C == 4) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr));
+  } else if constexpr (C == 8) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]) : "r"(taddr));
+  } else if constexpr (C == 16) {
+    float t[16];
+    tmem_ld16(taddr, t);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(t[i]);
+  } else {
+    static_assert(C == 32, "unsupported column count");
+    float t[16], u[16];
+    tmem_ld16(taddr, t);
+    tmem_ld16(taddr + 16, u);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      r[i] = __float_as_uint(t[i]);
+      r[16 + i] = __float_as_uint(u[i]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < C; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk, uint32_t region) {
+  return smem_desc_sw128(base + (kk >> 2) * region + (kk & 3) * 32, 16, 1024);
+}
+
+__device__ __forceinline__ uint64_t desc_v(uint32_t base, int kk) {
+  return smem_desc_sw128(base + kk * 2048, kRegion, 1024);
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int *abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
+__device__ __forceinline__ void st_shared_b16(uint32_t addr, float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  asm volatile("st.shared.b16 [%0], %1;" :: "r"(addr), "h"(*reinterpret_cast<const unsigned short *>(&h))
+               : "memory");
+}
+
+// T: tokens per stage (128 / Hkv); G: query heads per KV head.
+template <int T, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const GParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_addr);
+  const GLayout L = g_layout(p.stages, p.n_cols);
+  const int N = p.n_cols;
+  const int S = p.stages;
+  const uint32_t small = N * 128;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int total = reinterpret_cast<const int *>(p.ws)[0];
+  const int range = reinterpret_cast<const int *>(p.ws)[1];
+  const int *cu = reinterpret_cast<const int *>(p.ws + 256);
+  const int lo = static_cast<int>(blockIdx.x) * range;
+  const int hi = min(lo + range, total);
+
+  const uint32_t bar0 = base + L.bar;
+  auto kv_full = [&](int s) { return bar0 + 8u * s; };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto s_full = [&](int b) { return bar0 + 8u * (8 + b); };
+  auto s_free = [&](int b) { return bar0 + 8u * (10 + b); };
+  const uint32_t p_full = bar0 + 8u * 12;
+  const uint32_t pv_done = bar0 + 8u * 13;
+  const uint32_t x_bar = bar0 + 8u * 14;    // per-stage exchange among the softmax warps
+  const uint32_t l_bar = bar0 + 8u * 15;    // per-segment row-sum exchange
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bar + 16 * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  GDesc *desc = reinterpret_cast<GDesc *>(smem + L.desc);
+  float *alpha_buf = reinterpret_cast<float *>(smem + L.alpha);          // [2][kMaxN]
+  volatile int *grow_flag = reinterpret_cast<volatile int *>(alpha_buf + 2 * kMaxN);  // [2]
+  float *lsum_buf = reinterpret_cast<float *>(smem + L.lsum);
+  float *msum_buf = reinterpret_cast<float *>(smem + L.msum);
+  const uint32_t sK = base + L.k, sV = base + L.v, sQ = base + L.q, sP = base + L.p;
+
+  // Q^T and P^T padding rows/columns must read as zeros for the whole kernel
+  for (int i = threadIdx.x; i < (6 * static_cast<int>(small)) / 16; i += kThreads)
+    reinterpret_cast<uint4 *>(smem + L.q)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x < 2) grow_flag[threadIdx.x] = 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_free(b), 4);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
+    mbar_init(x_bar, 4);
+    mbar_init(l_bar, 4);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), p.tmem_cols);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_o = tmem;                       // O^T: columns [0, N)
+  auto tmem_s = [&](int b) { return tmem + N * (1 + b); };  // S^T buffers
+  auto fail = [&]() {
+    *abort_flag = 1;
+    raise_error(p.err, PKV_DEVERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // --------------------------------------------------------------- producer
+    int issued = 0, segs = 0;
+    bool ok = true;
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+    auto stage = [&](const GDesc &d, int blk_row, bool with_q) -> bool {
+      const int s = issued % S;
+      const int round = issued / S;
+      int good = 1;
+      if (lane == 0) {
+        if (round > 0 && !mbar_wait(kv_empty(s), (round - 1) & 1, abort_flag)) {
+          good = 0;
+          fail();
+        } else {
+          desc[s] = d;
+          const bool load = !(d.flags & kEnd) && blk_row >= 0;
+          const uint32_t bytes = (load ? 4 * kRegion : 0) + (with_q ? 2 * p.num_q_heads * 128 : 0);
+          if (bytes) mbar_arrive_expect_tx(kv_full(s), bytes);
+          else mbar_arrive(kv_full(s));
+          if (with_q) {
+            const uint32_t qdst = sQ + d.qbuf * 2 * small;
+            tma_load_3d(qdst, &tm_q, 0, 0, d.seq, kv_full(s));
+            tma_load_3d(qdst + small, &tm_q, 64, 0, d.seq, kv_full(s));
+          }
+          if (load) {
+            const uint32_t kd = sK + s * kKVBytes, vd = sV + s * kKVBytes;
+            tma_load_3d(kd, &tm_k, 0, blk_row, 0, kv_full(s));
+            tma_load_3d(kd + kRegion, &tm_k, 64, blk_row, 0, kv_full(s));
+            tma_load_3d(vd, &tm_v, 0, blk_row, 0, kv_full(s));
+            tma_load_3d(vd + kRegion, &tm_v, 64, blk_row, 0, kv_full(s));
+          }
+        }
+      }
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (good) ++issued;
+      return good != 0;
+    };
+
+    if (lo < hi) {
+      int a = 0, b = p.num_seqs - 1;
+      while (a < b) {
+        const int m = (a + b) >> 1;
+        if (cu[m + 1] > lo) b = m; else a = m + 1;
+      }
+      for (int i = a; ok && i < p.num_seqs; ++i) {
+        const int c0 = cu[i], c1 = cu[i + 1];
+        if (c0 >= hi) break;
+        if (c1 == c0) continue;
+        GDesc d;
+        d.seq = i;
+        d.p0 = max(lo, c0) - c0;
+        d.p1 = min(hi, c1) - c0;
+        const bool complete = c0 >= lo && c1 <= hi;
+        d.slot = complete ? -1 : (c0 <= lo ? 2 * int(blockIdx.x) : 2 * int(blockIdx.x) + 1);
+        d.qbuf = segs & 1;
+        d.pad = 0;
+        const int32_t *row = p.block_tables + static_cast<size_t>(i) * p.max_blocks_per_seq;
+        int cached = -(1 << 30), my_id = -1;
+        bool first = true;
+        for (int pa = d.p0 - d.p0 % T; ok && pa < d.p1; pa += T) {
+          const int lb = pa / p.block_size;
+          if (lb < cached || lb >= cached + 32) {  // window of 32 block ids, one per lane
+            cached = lb;
+            my_id = lb + lane < p.max_blocks_per_seq ? __ldg(row + lb + lane) : -1;
+          }
+          const int blk = __shfl_sync(0xffffffffu, my_id, lb - cached);
+          int blk_row = -1;
+          if (blk >= 0 && blk < p.num_blocks) {
+            blk_row = blk * p.block_size + (pa - lb * p.block_size);
+          } else if (lane == 0) {
+            raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+          }
+          d.pa = pa;
+          d.flags = (first ? kFirst : 0) | (pa + T >= d.p1 ? kLast : 0);
+          ok = stage(d, blk_row, first);
+          first = false;
+        }
+        ++segs;
+      }
+    }
+    if (ok) {
+      GDesc e;
+      e.seq = e.pa = e.p0 = e.p1 = e.slot = e.qbuf = e.pad = 0;
+      e.flags = kEnd;
+      ok = stage(e, -1, false);
+    }
+    if (lane == 0) {
+      for (int j = max(0, issued - S); j < issued; ++j)
+        mbar_wait(kv_full(j % S), (j / S) & 1, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = umma_idesc_bf16(kRows, N, false);
+      const uint32_t idesc_pv = umma_idesc_bf16(kHD, N, false) | (1u << 15);  // A (V) MN-major
+      bool ok = true;
+      int pv_issued = 0, s_issued = 0;
+      int prev_s = 0, prev_first = 0;
+      auto issue_pv = [&](int t, int s, int first) -> bool {
+        if (!mbar_wait(p_full, t & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk)
+          umma_bf16(tmem_o, desc_v(sV + s * kKVBytes, kk), desc_k(sP, kk, small), idesc_pv,
+                    (first && kk == 0) ? 0u : 1u);
+        umma_commit(pv_done);
+        umma_commit(kv_empty(s));
+        ++pv_issued;
+        return true;
+      };
+      for (int j = 0;; ++j) {
+        const int s = j % S;
+        if (!mbar_wait(kv_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
+        const GDesc d = desc[s];
+        if (d.flags & kEnd) break;
+        const int buf = j & 1;
+        if (j >= 2 && !mbar_wait(s_free(buf), ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t q = sQ + d.qbuf * 2 * small;
+#pragma unroll
+        for (int kk = 0; kk < kHD / 16; ++kk)
+          umma_bf16(tmem_s(buf), desc_k(sK + s * kKVBytes, kk, kRegion), desc_k(q, kk, small),
+                    idesc_s, kk > 0 ? 1u : 0u);
+        umma_commit(s_full(buf));
+        ++s_issued;
+        if (j > 0 && !issue_pv(j - 1, prev_s, prev_first)) { ok = false; break; }
+        prev_s = s;
+        prev_first = (d.flags & kFirst) ? 1 : 0;
+      }
+      if (ok && s_issued > pv_issued) ok = issue_pv(s_issued - 1, prev_s, prev_first);
+      if (!ok) fail();
+      if (s_issued > 0) mbar_wait(s_full((s_issued - 1) & 1), ((s_issued - 1) >> 1) & 1, nullptr);
+      if (pv_issued > 0) mbar_wait(pv_done, (pv_issued - 1) & 1, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------------- softmax
+    const int quad = warp & 3;                  // TMEM lane quadrant of this warp
+    const int r = quad * 32 + lane;             // stage row (S^T lane) and dim (O^T lane)
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int head = r / T;                     // KV head of this row
+    const int t = r - head * T;                 // token of this row inside the stage
+    constexpr int kHeadsInWarp = 32 / T;
+    constexpr int kCols = kHeadsInWarp * G;   // S^T columns of the heads of this warp
+    const int warp_head0 = (quad * 32) / T;
+    const int my_slot = head - warp_head0;      // which of the warp's heads this lane's row is
+    float m_used[G], l_part[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m_used[g] = -INFINITY;
+      l_part[g] = 0.f;
+    }
+    int segs_done = 0;
+    bool ok = true;
+    // P^T (N rows x 128 stage rows, K-major, 128-byte swizzle): element (n, r)
+    const uint32_t p_region = sP + (r >> 6) * small;
+    const int rc = r & 63;
+    for (int j = 0;; ++j) {
+      const int s = j % S;
+      if (!warp_wait(kv_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
+      const GDesc d = desc[s];
+      if (d.flags & kEnd) break;
+      const int buf = j & 1;
+      const bool first = (d.flags & kFirst) != 0;
+      if (!warp_wait(s_full(buf), (j >> 1) & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      // the S^T columns of all heads of this warp in one load; keep this row's G
+      float cols[kCols];
+      tmem_ld_cols<kCols>(tmem_s(buf) + lane_off + warp_head0 * G, cols);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(buf));
+      float sc[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float v = cols[g];
+#pragma unroll
+        for (int k = 1; k < kHeadsInWarp; ++k) v = (my_slot == k) ? cols[k * G + g] : v;
+        sc[g] = v;
+      }
+
+      const int tok = d.pa + t;
+      const bool valid = tok >= d.p0 && tok < d.p1;
+      float vmax[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        sc[g] = valid ? sc[g] * p.scale_log2 : -INFINITY;
+        vmax[g] = sc[g];
+      }
+      // stage maximum of each query head over the T rows of its KV head (one warp)
+#pragma unroll
+      for (int off = T >> 1; off >= 1; off >>= 1)
+#pragma unroll
+        for (int g = 0; g < G; ++g) vmax[g] = fmaxf(vmax[g], __shfl_xor_sync(0xffffffffu, vmax[g], off));
+      float alpha[G];
+      bool grow = false;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        alpha[g] = 1.f;
+        if (first) {
+          m_used[g] = vmax[g];
+        } else if (vmax[g] > m_used[g] + kRescaleThreshold) {
+          alpha[g] = ex2(m_used[g] - vmax[g]);
+          m_used[g] = vmax[g];
+          grow = true;
+        }
+      }
+      // P^T values and running row sums
+      float pr[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        pr[g] = valid ? ex2(sc[g] - m_used[g]) : 0.f;
+        l_part[g] = first ? pr[g] : l_part[g] * alpha[g] + pr[g];
+      }
+      // the previous PV must be done before P^T is rewritten or O^T rescaled
+      if (j > 0) {
+        if (!warp_wait(pv_done, (j - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int n = head * G + g;
+        st_shared_b16(p_region + (n >> 3) * 1024 + (n & 7) * 128 +
+                          ((((rc >> 3) ^ (n & 7)) << 4) | ((rc & 7) << 1)),
+                      pr[g]);
+      }
+      if (!valid) {  // masked row: its V row must be zero for the PV MMA
+        const uint32_t vrow = sV + s * kKVBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" :: "r"(vrow + c * 16), "r"(0u) : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" :: "r"(vrow + kRegion + c * 16), "r"(0u) : "memory");
+        }
+      }
+      // broadcast the rare O^T rescale of the heads whose maximum grew
+      float *abuf = alpha_buf + (j & 1) * kMaxN;
+      if (t == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) abuf[head * G + g] = alpha[g];
+        if (grow) grow_flag[j & 1] = j + 1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(x_bar);
+      if (!warp_wait(x_bar, j & 1, abort_flag)) { ok = false; break; }
+      if (grow_flag[j & 1] == j + 1) {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          float o[16];
+          tmem_ld16(tmem_o + lane_off + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (c0 + e < p.num_q_heads) o[e] *= abuf[c0 + e];
+          asm volatile(
+              "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+              "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+              :: "r"(tmem_o + lane_off + c0), "f"(o[0]), "f"(o[1]), "f"(o[2]), "f"(o[3]),
+                 "f"(o[4]), "f"(o[5]), "f"(o[6]), "f"(o[7]), "f"(o[8]), "f"(o[9]), "f"(o[10]),
+                 "f"(o[11]), "f"(o[12]), "f"(o[13]), "f"(o[14]), "f"(o[15])
+              : "memory");
+        }
+        tmem_wait_st();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+
+      if (d.flags & kLast) {
+        // row sums of each query head: sum over the T rows of its KV head
+        float ls[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) ls[g] = l_part[g];
+#pragma unroll
+        for (int off = T >> 1; off >= 1; off >>= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) ls[g] += __shfl_xor_sync(0xffffffffu, ls[g], off);
+        if (t == 0) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            lsum_buf[head * G + g] = ls[g];
+            msum_buf[head * G + g] = m_used[g];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(l_bar);
+        if (!warp_wait(l_bar, segs_done & 1, abort_flag)) { ok = false; break; }
+        if (!warp_wait(pv_done, j & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        // O^T lane r is output dim r: write every query head's value of this dim
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          float o[16];
+          tmem_ld16(tmem_o + lane_off + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int n = c0 + e;
+            if (n < p.num_q_heads) {
+              const float l = lsum_buf[n];
+              const float v = l > 0.f ? o[e] / l : 0.f;
+              if (d.slot < 0) {
+                p.out[(static_cast<size_t>(d.seq) * p.num_q_heads + n) * kHD + r] = __float2bfloat16_rn(v);
+              } else {
+                const size_t rec = static_cast<size_t>(d.slot) * p.num_q_heads + n;
+                p.po[rec * kHD + r] = v;
+                if (r == 0) p.ml[rec] = make_float2(msum_buf[n], l);
+              }
+            }
+          }
+        }
+        ++segs_done;
+      }
+    }
+    if (!ok) fail();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap *map, const void *ptr, const cuuint64_t (&dims)[3],
+            const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3]) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+using TcgKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const GParams);
+
+template <int T>
+TcgKernel tcg_kernel_for_g(int g) {
+  switch (g) {
+    case 1: return decode_tcg_kernel<T, 1>;
+    case 2: return decode_tcg_kernel<T, 2>;
+    case 4: return decode_tcg_kernel<T, 4>;
+    case 8: return decode_tcg_kernel<T, 8>;
+    default: return nullptr;
+  }
+}
+
+// instantiated shapes: T in {8, 16, 32} (Hkv 16, 8, 4), G in {1, 2, 4, 8}
+TcgKernel tcg_kernel_for(int t, int g) {
+  switch (t) {
+    case 8: return tcg_kernel_for_g<8>(g);
+    case 16: return tcg_kernel_for_g<16>(g);
+    case 32: return tcg_kernel_for_g<32>(g);
+    default: return nullptr;
+  }
+}
+
+int pick_stages(int n_cols) {
+  for (int s = 3; s >= 2; --s)
+    if (g_layout(s, n_cols).total + 1024 <= 227 * 1024) return s;
+  return 0;
+}
+
+}  // namespace
+
+bool decode_tcg_supported(int num_q_heads, int num_kv_heads, int block_size) {
+  if (num_kv_heads != 4 && num_kv_heads != 8 && num_kv_heads != 16) return false;
+  if (num_q_heads % num_kv_heads != 0) return false;
+  if (tcg_kernel_for(kRows / num_kv_heads, num_q_heads / num_kv_heads) == nullptr) return false;
+  const int n_cols = (num_q_heads + 15) / 16 * 16;
+  if (n_cols > kMaxN) return false;
+  const int T = kRows / num_kv_heads;
+  return block_size % T == 0 && pick_stages(n_cols) > 0;
+}
+
+cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *po,
+                              cudaStream_t stream) {
+  const int n_cols = (a.num_q_heads + 15) / 16 * 16;
+  const int stages = pick_stages(n_cols);
+  const size_t smem = g_layout(stages, n_cols).total + 1024;
+  cudaError_t e = cudaSuccess;
+  const int T = kRows / a.num_kv_heads;
+  CUtensorMap tq, tk, tv;
+  const cuuint64_t cache_rows = static_cast<cuuint64_t>(a.num_blocks) * a.block_size;
+  const cuuint64_t hkv = a.num_kv_heads;
+  // q as (dim, head, sequence): one box = all query heads of a sequence, one 64-dim half
+  const cuuint64_t qd[3] = {kHD, static_cast<cuuint64_t>(a.num_q_heads), static_cast<cuuint64_t>(a.num_seqs)};
+  const cuuint64_t qs[2] = {kHD * 2, static_cast<cuuint64_t>(a.num_q_heads) * kHD * 2};
+  const cuuint32_t qb[3] = {64, static_cast<cuuint32_t>(a.num_q_heads), 1};
+  // cache as (dim, token row, head): one box = T tokens x all heads, one 64-dim half
+  const cuuint64_t cd[3] = {kHD, cache_rows, hkv};
+  const cuuint64_t cs[2] = {hkv * kHD * 2, kHD * 2};
+  const cuuint32_t cb[3] = {64, static_cast<cuuint32_t>(T), static_cast<cuuint32_t>(hkv)};
+  if (!encode(&tq, a.q, qd, qs, qb) || !encode(&tk, a.k_cache, cd, cs, cb) ||
+      !encode(&tv, a.v_cache, cd, cs, cb))
+    return cudaErrorInvalidValue;
+  int tmem_cols = 32;
+  while (tmem_cols < 3 * n_cols + 16) tmem_cols <<= 1;
+  GParams p;
+  p.out = static_cast<__nv_bfloat16 *>(a.out);
+  p.block_tables = a.block_tables;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = a.num_q_heads / a.num_kv_heads;
+  p.n_cols = n_cols;
+  p.tokens = T;
+  p.block_size = a.block_size;
+  p.num_blocks = a.num_blocks;
+  p.stages = stages;
+  p.tmem_cols = tmem_cols;
+  p.scale_log2 = a.scale * kLog2e;
+  p.ws = static_cast<const uint8_t *>(a.workspace);
+  p.ml = ml;
+  p.po = po;
+  p.err = a.err;
+  auto kern = tcg_kernel_for(T, p.group);
+  if (kern == nullptr) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

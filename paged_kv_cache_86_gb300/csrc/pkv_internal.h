@@ -42,11 +42,34 @@ struct DecodeArgs {
   uint32_t *err;
 };
 
-// Grid size (CTAs) of the split-decode kernel for this head configuration on
-// the current device, or 0 if the configuration is unsupported.
-int decode_grid(int num_q_heads, int num_kv_heads, cudaError_t *status);
-size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int grid);
-cudaError_t launch_paged_decode(const DecodeArgs &a, int grid, cudaStream_t stream);
+// Which decode kernel runs and on how many CTAs. Block sizes that are a
+// multiple of 8 (and at most 16 query heads per KV head) run the tcgen05
+// kernel; other shapes the CUDA-core split kernel.
+struct DecodePlan {
+  int kind;  // 3: tcgen05, all KV heads per stage; 2: tcgen05, one KV head per CTA range; 1: CUDA cores
+  bool tc;   // records keyed by (slot, query head of the group) -- kind 2 only
+  int grid;
+};
+
+bool choose_decode_plan(int num_q_heads, int num_kv_heads, int block_size, DecodePlan *plan,
+                        cudaError_t *status);
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                              const DecodePlan &plan);
+// The largest workspace any block size needs for this head configuration.
+size_t decode_workspace_upper_bound(int num_seqs, int num_q_heads, int num_kv_heads,
+                                    cudaError_t *status);
+cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
+
+// tcgen05 decode kernel, all KV heads of a block per stage (decode_tcg.cu)
+bool decode_tcg_supported(int num_q_heads, int num_kv_heads, int block_size);
+cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *po,
+                              cudaStream_t stream);
+
+// tcgen05 decode kernel, one KV head per CTA range (decode_tc.cu)
+bool decode_tc_supported(int num_q_heads, int num_kv_heads, int block_size);
+int decode_tc_grid();
+cudaError_t launch_decode_tc(const DecodeArgs &a, int grid, float2 *ml, float *po,
+                             cudaStream_t stream);
 
 // ---- prefill
 struct PrefillArgs {

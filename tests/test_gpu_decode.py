@@ -54,6 +54,19 @@ def test_decode_head_configurations(hkv, group):
     check(w)
 
 
+@pytest.mark.parametrize("hkv,group,bs", [(16, 1, 16), (3, 5, 32), (2, 16, 16), (1, 12, 8),
+                                           (8, 4, 12), (4, 4, 6), (4, 4, 32), (32, 2, 16),
+                                           (8, 3, 16), (16, 8, 16), (64, 1, 16)])
+def test_decode_more_head_shapes(hkv, group, bs):
+    # all-heads tcgen05 kernel when Hkv is a power of two >= 4 and 128/Hkv divides
+    # the block size; per-head tcgen05 kernel for other block sizes that are
+    # multiples of 8; the CUDA-core split kernel for the rest
+    lens = [1, 9, 128, 129, 700, 2000]
+    w = W.decode_workload(f"shape_{hkv}x{group}_bs{bs}", lens, hkv * group, hkv, bs,
+                          seed=500 + hkv * 31 + group * 7 + bs)
+    check(w)
+
+
 @pytest.mark.parametrize("bs", [1, 3, 8, 64, 256, 1024])
 def test_decode_block_sizes(bs):
     w = W.decode_workload(f"bs{bs}", [5, 300, 1, 1024, 77], 32, 8, bs, seed=200 + bs)
