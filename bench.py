@@ -158,20 +158,23 @@ def store_bytes(w) -> int:
     return int(w.num_new_tokens * (2 * w.num_kv_heads * w.head_dim * 2 * 2 + 4))
 
 
-def source_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_hash(paths):
+    m = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            m.update(f.read())
+    return m.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_source, name):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source; otherwise None."""
+def profiled_traffic(name):
+    """DRAM bytes (read + write) per decode call from the committed ncu launch
+    list, if it was taken on the current kernel sources; otherwise None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(name)
-    if not rec or rec.get("source_sha256_16") != source_hash(kernel_source):
+    if not rec or rec.get("source_sha256_16") != source_hash(rec.get("sources", [])):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -357,8 +360,7 @@ def run_pkv(args, rank, world, device):
         "roofline": {"bound": "hbm", "kernel": "pkv_paged_decode (plan + split + combine)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": profiled_traffic(os.path.join(ROOT, "paged_kv_cache_86_gb300", "csrc",
-                                                              "decode.cu"), w.name),
+                     "traffic": profiled_traffic(w.name),
                      "algorithmic_bytes_per_launch": dbytes, "launch_ms": decode_ms},
         "ops": {"store_ms": store_ms, "store_gbs": store_bytes(w) / (store_ms * 1e-3) / 1e9,
                 "decode_ms": decode_ms},

@@ -51,7 +51,7 @@ constexpr int kRows = 128;            // MMA M: rows of a stage (T tokens x Hkv 
 constexpr int kHD = 128;
 constexpr int kRegion = 16384;        // 128 rows x 128 B (one 64-dim half)
 constexpr int kKVBytes = 2 * kRegion;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;  // K producer, MMA, 4 softmax warps, V producer
 constexpr int kMaxN = 128;
 constexpr int kMaxG = 16;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -101,7 +101,7 @@ __host__ __device__ inline GLayout g_layout(int stages, int n_cols) {
   L.msum = L.lsum + kMaxN * 4;            // [kMaxN] maxima
   L.desc = L.msum + kMaxN * 4;
   L.bar = L.desc + 4 * 32;
-  L.total = L.bar + 16 * 8 + 16;
+  L.total = L.bar + 24 * 8 + 16;
   return L;
 }
 
@@ -201,15 +201,20 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int hi = min(lo + range, total);
 
   const uint32_t bar0 = base + L.bar;
-  auto kv_full = [&](int s) { return bar0 + 8u * s; };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (4 + s); };
+  // K and V have their own rings: a K slot is free once S has been computed
+  // from it and the softmax warps have read its stage descriptor; a V slot once
+  // the PV MMA that reads it has completed
+  auto k_full = [&](int s) { return bar0 + 8u * s; };
+  auto k_empty = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (16 + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (20 + s); };
   auto s_full = [&](int b) { return bar0 + 8u * (8 + b); };
   auto s_free = [&](int b) { return bar0 + 8u * (10 + b); };
   const uint32_t p_full = bar0 + 8u * 12;
   const uint32_t pv_done = bar0 + 8u * 13;
   const uint32_t x_bar = bar0 + 8u * 14;    // per-stage exchange among the softmax warps
   const uint32_t l_bar = bar0 + 8u * 15;    // per-segment row-sum exchange
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bar + 16 * 8);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bar + 24 * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   GDesc *desc = reinterpret_cast<GDesc *>(smem + L.desc);
   float *alpha_buf = reinterpret_cast<float *>(smem + L.alpha);          // [2][kMaxN]
@@ -224,8 +229,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (threadIdx.x < 2) grow_flag[threadIdx.x] = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1 + 4);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
@@ -254,45 +261,66 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     raise_error(p.err, PKV_DEVERR_TIMEOUT);
   };
 
-  if (warp == 0) {
-    // --------------------------------------------------------------- producer
+  if (warp == 0 || warp == 6) {
+    // -------------------------------------------------------------- producers
+    // Both walk the same stages; warp 0 loads K (and Q, and writes the stage
+    // descriptors), warp 6 loads V.
+    const bool is_k = warp == 0;
     int issued = 0, segs = 0;
+    int q_last[2] = {-1, -1};  // last stage whose S MMA reads each Q^T buffer
     bool ok = true;
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
+      if (is_k) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+      } else {
+        tma_prefetch_desc(&tm_v);
+      }
     }
     auto stage = [&](const GDesc &d, int blk_row, bool with_q) -> bool {
       const int s = issued % S;
       const int round = issued / S;
       int good = 1;
       if (lane == 0) {
-        if (round > 0 && !mbar_wait(kv_empty(s), (round - 1) & 1, abort_flag)) {
+        const uint32_t empty = is_k ? k_empty(s) : v_empty(s);
+        const uint32_t full = is_k ? k_full(s) : v_full(s);
+        // a Q^T buffer may only be refilled once the S MMAs of the previous
+        // segment that used it are done (the slot wait covers stage issued - S)
+        const int prev_q = (is_k && with_q) ? q_last[d.qbuf] : -1;
+        if (prev_q >= 0 && prev_q > issued - S &&
+            !mbar_wait(k_empty(prev_q % S), (prev_q / S) & 1, abort_flag)) {
+          good = 0;
+          fail();
+        } else if (round > 0 && !mbar_wait(empty, (round - 1) & 1, abort_flag)) {
           good = 0;
           fail();
         } else {
-          desc[s] = d;
           const bool load = !(d.flags & kEnd) && blk_row >= 0;
-          const uint32_t bytes = (load ? 4 * kRegion : 0) + (with_q ? 2 * p.num_q_heads * 128 : 0);
-          if (bytes) mbar_arrive_expect_tx(kv_full(s), bytes);
-          else mbar_arrive(kv_full(s));
-          if (with_q) {
+          uint32_t bytes = load ? 2 * kRegion : 0;
+          if (is_k) {
+            desc[s] = d;
+            if (with_q) bytes += 2 * p.num_q_heads * 128;
+          }
+          if (bytes) mbar_arrive_expect_tx(full, bytes);
+          else mbar_arrive(full);
+          if (is_k && with_q) {
             const uint32_t qdst = sQ + d.qbuf * 2 * small;
-            tma_load_3d(qdst, &tm_q, 0, 0, d.seq, kv_full(s));
-            tma_load_3d(qdst + small, &tm_q, 64, 0, d.seq, kv_full(s));
+            tma_load_3d(qdst, &tm_q, 0, 0, d.seq, full);
+            tma_load_3d(qdst + small, &tm_q, 64, 0, d.seq, full);
           }
           if (load) {
-            const uint32_t kd = sK + s * kKVBytes, vd = sV + s * kKVBytes;
-            tma_load_3d(kd, &tm_k, 0, blk_row, 0, kv_full(s));
-            tma_load_3d(kd + kRegion, &tm_k, 64, blk_row, 0, kv_full(s));
-            tma_load_3d(vd, &tm_v, 0, blk_row, 0, kv_full(s));
-            tma_load_3d(vd + kRegion, &tm_v, 64, blk_row, 0, kv_full(s));
+            const uint32_t dst = (is_k ? sK : sV) + s * kKVBytes;
+            const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+            tma_load_3d(dst, map, 0, blk_row, 0, full);
+            tma_load_3d(dst + kRegion, map, 64, blk_row, 0, full);
           }
         }
       }
       good = __shfl_sync(0xffffffffu, good, 0);
-      if (good) ++issued;
+      if (good) {
+        if (!(d.flags & kEnd)) q_last[d.qbuf] = issued;
+        ++issued;
+      }
       return good != 0;
     };
 
@@ -327,7 +355,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           int blk_row = -1;
           if (blk >= 0 && blk < p.num_blocks) {
             blk_row = blk * p.block_size + (pa - lb * p.block_size);
-          } else if (lane == 0) {
+          } else if (lane == 0 && is_k) {
             raise_error(p.err, PKV_DEVERR_BLOCK_ID);
           }
           d.pa = pa;
@@ -344,9 +372,9 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       e.flags = kEnd;
       ok = stage(e, -1, false);
     }
-    if (lane == 0) {
+    if (lane == 0) {  // drain: the last copies must land before the CTA exits
       for (int j = max(0, issued - S); j < issued; ++j)
-        mbar_wait(kv_full(j % S), (j / S) & 1, nullptr);
+        mbar_wait(is_k ? k_full(j % S) : v_full(j % S), (j / S) & 1, nullptr);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -357,6 +385,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       int pv_issued = 0, s_issued = 0;
       int prev_s = 0, prev_first = 0;
       auto issue_pv = [&](int t, int s, int first) -> bool {
+        if (!mbar_wait(v_full(s), (t / S) & 1, abort_flag)) return false;
         if (!mbar_wait(p_full, t & 1, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
@@ -364,13 +393,13 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           umma_bf16(tmem_o, desc_v(sV + s * kKVBytes, kk), desc_k(sP, kk, small), idesc_pv,
                     (first && kk == 0) ? 0u : 1u);
         umma_commit(pv_done);
-        umma_commit(kv_empty(s));
+        umma_commit(v_empty(s));
         ++pv_issued;
         return true;
       };
       for (int j = 0;; ++j) {
         const int s = j % S;
-        if (!mbar_wait(kv_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(k_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
         const GDesc d = desc[s];
         if (d.flags & kEnd) break;
         const int buf = j & 1;
@@ -382,6 +411,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           umma_bf16(tmem_s(buf), desc_k(sK + s * kKVBytes, kk, kRegion), desc_k(q, kk, small),
                     idesc_s, kk > 0 ? 1u : 0u);
         umma_commit(s_full(buf));
+        umma_commit(k_empty(s));
         ++s_issued;
         if (j > 0 && !issue_pv(j - 1, prev_s, prev_first)) { ok = false; break; }
         prev_s = s;
@@ -417,8 +447,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int rc = r & 63;
     for (int j = 0;; ++j) {
       const int s = j % S;
-      if (!warp_wait(kv_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
+      if (!warp_wait(k_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
       const GDesc d = desc[s];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(k_empty(s));  // this stage's descriptor has been read
       if (d.flags & kEnd) break;
       const int buf = j & 1;
       const bool first = (d.flags & kFirst) != 0;
@@ -485,6 +517,8 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                           ((((rc >> 3) ^ (n & 7)) << 4) | ((rc & 7) << 1)),
                       pr[g]);
       }
+      const bool partial = d.pa < d.p0 || d.pa + T > d.p1;
+      if (partial && !warp_wait(v_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
       if (!valid) {  // masked row: its V row must be zero for the PV MMA
         const uint32_t vrow = sV + s * kKVBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
