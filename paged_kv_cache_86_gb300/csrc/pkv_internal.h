@@ -97,4 +97,8 @@ struct PrefillArgs {
 bool prefill_supported(int num_q_heads, int num_kv_heads, int block_size);
 cudaError_t launch_paged_prefill(const PrefillArgs &a, cudaStream_t stream);
 
+// two query heads per CTA in ping-pong (prefill_pp.cu): even GQA groups
+bool prefill_pp_supported(int num_q_heads, int num_kv_heads, int block_size);
+cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream);
+
 }  // namespace pkv

@@ -454,6 +454,8 @@ bool prefill_supported(int num_q_heads, int num_kv_heads, int block_size) {
 
 cudaError_t launch_paged_prefill(const PrefillArgs &a, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.total_q == 0 || a.max_seqlen_q == 0) return cudaSuccess;
+  if (prefill_pp_supported(a.num_q_heads, a.num_kv_heads, a.block_size))
+    return launch_prefill_pp(a, stream);
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {

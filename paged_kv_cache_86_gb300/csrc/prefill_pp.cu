@@ -1,0 +1,512 @@
+// prefill_pp.cu -- paged chunked-prefill attention, two query heads per CTA in
+// ping-pong on the tcgen05 tensor cores (sm_103a).
+//
+// Same computation as prefill.cu (varlen query chunks over their cached prefix
+// plus themselves, bottom-right causal; nano vllm代码详解 §2 context;
+// 推理运行时 §Prefill 与 decode 输入; Mini-SGLang 源码解析（二）§6.6), and the
+// same compute-bound regime (Mini-SGLang 源码解析（二）§8.3). What changes is
+// the schedule, so that the tensor core never waits for a softmax:
+//
+//   * One CTA = one 128-row query tile of TWO query heads A and B of the same
+//     KV head (GQA): the K and V tiles are loaded once for both.
+//   * Two softmax warpgroups (warps 2-5 for A, 6-9 for B). While one computes
+//     the softmax of its tile, the tensor core runs the other head's S and PV.
+//     MMA issue order per KV tile j: PV_A(j-1), S_A(j), PV_B(j-1), S_B(j).
+//   * All four accumulators live in TMEM (S_A, S_B, O_A, O_B: 4 x 128 columns,
+//     the whole TMEM of the SM). P is written back as bf16 over the first 64
+//     columns of its S and fed to the PV MMA as the A operand straight from
+//     TMEM, so shared memory only holds Q_A, Q_B and two K and two V stages.
+//   * The softmax works on raw scores (max of s, then exp2(s*c - m*c) with one
+//     FFMA per element, c = scale * log2 e) and rescales O lazily: only when a
+//     row's maximum grows by more than 2^8 (in units of c), so O stays valid
+//     and P <= 256 fits bf16. A rescale needs no extra wait: S_X(j) completing
+//     implies PV_X(j-1) completed (the tensor core runs one CTA's MMAs in order).
+//
+// Every wait is bounded; on a timeout the CTA records PKV_DEVERR_TIMEOUT,
+// drains its copies and MMAs, frees its TMEM and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+#include "pkv_tc.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kHD = 128;
+constexpr int kRegion = 16384;
+constexpr int kTileBytes = 2 * kRegion;
+constexpr int kStages = 2;
+constexpr int kThreads = 320;        // TMA, MMA, softmax A (4 warps), softmax B (4 warps)
+constexpr int kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.f;
+
+constexpr int kOffQ = 0;                              // Q_A, Q_B
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
+constexpr int kOffV = kOffK + kStages * kTileBytes;
+constexpr int kOffBar = kOffV + kStages * kTileBytes;
+constexpr int kNumBars = 1 + 4 * kStages + 6;         // q, k/v full/empty, s_full x2, p_full x2, pv_done x2
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+
+struct PPParams {
+  __nv_bfloat16 *out;
+  const int32_t *cu_q;
+  const int32_t *cu_k;
+  const int32_t *block_tables;
+  int max_blocks_per_seq;
+  int num_seqs;
+  int total_q;
+  int num_q_heads;
+  int group;
+  int block_size;
+  int num_blocks;
+  int max_seqlen_q;
+  int max_seqlen_k;
+  int causal;
+  int box_rows;
+  float scale_log2;
+  uint32_t *err;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_base, int kk) {
+  return smem_desc_sw128(tile_base + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024);
+}
+
+__device__ __forceinline__ uint64_t desc_v_mnmajor(uint32_t tile_base, int kk) {
+  return smem_desc_sw128(tile_base + kk * 2048, kRegion, 1024);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc], bf16 inputs, fp32 accumulator.
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32_u(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+      :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+         "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+         "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]),
+         "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+         "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int *abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const PPParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_addr);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int seq = blockIdx.z;
+  const int qh_a = 2 * blockIdx.y;       // query heads qh_a, qh_a + 1 share KV head qh_a / G
+  const int r0 = blockIdx.x * kTile;
+
+  const int q_begin = p.cu_q[seq], q_end = p.cu_q[seq + 1];
+  const int k_len = p.cu_k[seq + 1] - p.cu_k[seq];
+  const int q_len = q_end - q_begin;
+  if (q_len < 0 || q_len > p.max_seqlen_q || q_end > p.total_q || k_len < 0 ||
+      k_len > p.max_seqlen_k || (p.causal && q_len > k_len)) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, PKV_DEVERR_LENGTH);
+    return;
+  }
+  if (r0 >= q_len) return;
+  const int prefix = p.causal ? k_len - q_len : 0;
+  const int last_row = min(r0 + kTile - 1, q_len - 1);
+  const int key_end = p.causal ? min(prefix + last_row + 1, k_len) : k_len;
+  const int n_tiles = (key_end + kTile - 1) / kTile;
+  const int kvh = qh_a / p.group;
+
+  const uint32_t bar0 = base + kOffBar;
+  const uint32_t q_full = bar0;
+  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + kStages + s); };
+  auto k_empty = [&](int s) { return bar0 + 8u * (1 + 2 * kStages + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * kStages + s); };
+  auto s_full = [&](int x) { return bar0 + 8u * (1 + 4 * kStages + x); };
+  auto p_full = [&](int x) { return bar0 + 8u * (3 + 4 * kStages + x); };
+  auto pv_done = [&](int x) { return bar0 + 8u * (5 + 4 * kStages + x); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + kNumBars * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(s_full(x), 1);
+      mbar_init(p_full(x), 4);
+      mbar_init(pv_done(x), 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto tmem_s = [&](int x) { return tmem + x * kTile; };           // S_A, S_B (P over cols 0..63)
+  auto tmem_o = [&](int x) { return tmem + (2 + x) * kTile; };     // O_A, O_B
+  const uint32_t sQ = base + kOffQ;
+  auto sK = [&](int s) { return base + kOffK + s * kTileBytes; };
+  auto sV = [&](int s) { return base + kOffV + s * kTileBytes; };
+  auto fail = [&]() {
+    *abort_flag = 1;
+    raise_error(p.err, PKV_DEVERR_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    int k_issued = 0, v_issued = 0;
+    bool ok = true;
+    if (n_tiles > 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+        for (int x = 0; x < 2; ++x) {
+          tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, qh_a + x, q_begin + r0, q_full);
+          tma_load_3d(sQ + x * kTileBytes + kRegion, &tm_q, 64, qh_a + x, q_begin + r0, q_full);
+        }
+      }
+      const int R = p.box_rows;
+      const int pieces = kTile / R;
+      const int oob_row = p.num_blocks * p.block_size;
+      const int32_t *bt = p.block_tables + static_cast<size_t>(seq) * p.max_blocks_per_seq;
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int s = j % kStages;
+        const int round = j / kStages;
+        int row = oob_row;
+        if (lane < pieces) {
+          const int key = j * kTile + lane * R;
+          if (key < k_len) {
+            const int blk = __ldg(bt + key / p.block_size);
+            if (blk >= 0 && blk < p.num_blocks) row = blk * p.block_size + key % p.block_size;
+            else raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+          }
+        }
+        for (int which = 0; which < 2 && ok; ++which) {
+          const uint32_t full = which ? v_full(s) : k_full(s);
+          const uint32_t empty = which ? v_empty(s) : k_empty(s);
+          const uint32_t dst = which ? sV(s) : sK(s);
+          const CUtensorMap *map = which ? &tm_v : &tm_k;
+          int good = 1;
+          if (lane == 0) {
+            if (round > 0 && !mbar_wait(empty, (round - 1) & 1, abort_flag)) {
+              good = 0;
+              fail();
+            } else {
+              mbar_arrive_expect_tx(full, kTileBytes);
+            }
+          }
+          good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) {
+            ok = false;
+            break;
+          }
+          if (lane < pieces) {
+            tma_load_3d(dst + lane * R * 128, map, 0, kvh, row, full);
+            tma_load_3d(dst + kRegion + lane * R * 128, map, 64, kvh, row, full);
+          }
+          if (which) ++v_issued; else ++k_issued;
+        }
+      }
+      if (lane == 0) {  // drain: the last copies must land before the CTA exits
+        mbar_wait(q_full, 0, nullptr);
+        for (int j = max(0, k_issued - kStages); j < k_issued; ++j)
+          mbar_wait(k_full(j % kStages), (j / kStages) & 1, nullptr);
+        for (int j = max(0, v_issued - kStages); j < v_issued; ++j)
+          mbar_wait(v_full(j % kStages), (j / kStages) & 1, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t idesc_s = umma_idesc_bf16(kTile, kTile, false);
+      constexpr uint32_t idesc_pv = umma_idesc_bf16(kTile, kHD, true);  // B (V) MN-major
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      int s_commits[2] = {0, 0}, pv_commits[2] = {0, 0};
+      auto issue_s = [&](int x, int j) {
+        const int s = j % kStages;
+        const uint32_t q = sQ + x * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kHD / 16; ++kk)
+          umma_bf16(tmem_s(x), desc_kmajor(q, kk), desc_kmajor(sK(s), kk), idesc_s, kk > 0 ? 1u : 0u);
+        umma_commit(s_full(x));
+        ++s_commits[x];
+        if (x == 1) umma_commit(k_empty(s));   // K(j) has fed both heads
+      };
+      auto issue_pv = [&](int x, int j) -> bool {
+        const int s = j % kStages;
+        if (!mbar_wait(p_full(x), j & 1, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_bf16_tmem_a(tmem_o(x), tmem_s(x) + kk * 8, desc_v_mnmajor(sV(s), kk), idesc_pv,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(pv_done(x));
+        ++pv_commits[x];
+        if (x == 1) umma_commit(v_empty(s));   // V(j) has fed both heads
+        return true;
+      };
+      // S_A(0), S_B(0), then per tile: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+      if (ok) ok = mbar_wait(k_full(0), 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait(v_full(s), (j / kStages) & 1, abort_flag)) { ok = false; break; }
+        const bool more = j + 1 < n_tiles;
+        const int s1 = (j + 1) % kStages;
+        for (int x = 0; ok && x < 2; ++x) {
+          if (!issue_pv(x, j)) { ok = false; break; }
+          if (more) {
+            if (x == 0 && !mbar_wait(k_full(s1), ((j + 1) / kStages) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(x, j + 1);
+          }
+        }
+      }
+      if (!ok) fail();
+      for (int x = 0; x < 2; ++x) {  // every issued MMA completes before TMEM is freed
+        if (s_commits[x] > 0) mbar_wait(s_full(x), (s_commits[x] - 1) & 1, nullptr);
+        if (pv_commits[x] > 0) mbar_wait(pv_done(x), (pv_commits[x] - 1) & 1, nullptr);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------- softmax A / B
+    const int x = (warp - 2) >> 2;                   // 0: head A, 1: head B
+    const int quad = warp & 3;                       // TMEM lanes 32*quad .. 32*quad+31
+    const int r = quad * 32 + lane;                  // query row inside the tile
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int qpos = prefix + r0 + r;
+    const int visible = p.causal ? min(qpos + 1, k_len) : k_len;
+    const float c = p.scale_log2;
+    float m_used = -INFINITY, l_sum = 0.f;           // running max of raw scores, row sum
+    bool ok = true;
+
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      if (!warp_wait(s_full(x), j & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      float s[kTile];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        tmem_ld32(tmem_s(x) + lane_off + cc * 32, *reinterpret_cast<float(*)[32]>(s + cc * 32));
+      tmem_wait_ld();
+
+      const int key0 = j * kTile;
+      float mt = -INFINITY;
+      if (key0 + kTile <= visible) {
+#pragma unroll
+        for (int e = 0; e < kTile; ++e) mt = fmaxf(mt, s[e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kTile; ++e) {
+          s[e] = (key0 + e < visible) ? s[e] : -INFINITY;
+          mt = fmaxf(mt, s[e]);
+        }
+      }
+      // lazy rescale: only when the maximum grows by more than 2^8 after scaling
+      const bool grow = mt != -INFINITY && (m_used == -INFINITY || (mt - m_used) * c > kRescaleThreshold);
+      float alpha = 1.f;
+      if (grow) {
+        if (m_used != -INFINITY) {
+          alpha = ex2((m_used - mt) * c);
+          l_sum *= alpha;
+        }
+        m_used = mt;
+      }
+      // O_X holds PV_X(0..j-1), complete because S_X(j) completed after it; the
+      // TMEM loads and stores are warp-collective, so the whole warp takes part
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          float o[32];
+          tmem_ld32(tmem_o(x) + lane_off + cc * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(tmem_o(x) + lane_off + cc * 32, o);
+        }
+        tmem_wait_st();
+      }
+      // P = exp2(s*c - m*c) as bf16 pairs over TMEM columns 0..63 of S_X
+      const float mc = m_used * c;
+      float rs = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float a0 = ex2(fmaf(s[half * 64 + 2 * e], c, -mc));
+          const float a1 = ex2(fmaf(s[half * 64 + 2 * e + 1], c, -mc));
+          rs += a0 + a1;
+          pk[e] = float2_to_bf16x2(a0, a1);
+        }
+        tmem_st32_u(tmem_s(x) + lane_off + half * 32, pk);
+      }
+      l_sum += rs;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full(x));
+    }
+
+    if (!ok) fail();
+    // epilogue: O / l -> bf16 rows
+    const bool have = n_tiles > 0;
+    if (have && ok) {
+      ok = warp_wait(pv_done(x), (n_tiles - 1) & 1, abort_flag);
+      tc_fence_after();
+    }
+    const bool store = (r0 + r) < q_len;
+    __nv_bfloat16 *orow = p.out + (static_cast<size_t>(q_begin) + r0 + r) * p.num_q_heads * kHD +
+                          static_cast<size_t>(qh_a + x) * kHD;
+    const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      float o[32];
+      if (have && ok) {
+        tmem_ld32(tmem_o(x) + lane_off + cc * 32, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0.f;
+      }
+      if (store) {
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 v;
+          v.x = float2_to_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+          v.y = float2_to_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+          v.z = float2_to_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+          v.w = float2_to_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+          dst[q4] = v;
+        }
+      }
+    }
+    if (!ok) fail();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t heads, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHD), heads, rows};
+  cuuint64_t strides[2] = {kHD * 2, heads * kHD * 2};
+  cuuint32_t box[3] = {64, 1, box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool prefill_pp_supported(int num_q_heads, int num_kv_heads, int block_size) {
+  return num_kv_heads >= 1 && num_q_heads % num_kv_heads == 0 &&
+         (num_q_heads / num_kv_heads) % 2 == 0 && block_size % 8 == 0;
+}
+
+cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(prefill_pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  int box_rows = a.block_size & -a.block_size;
+  if (box_rows > kTile) box_rows = kTile;
+  CUtensorMap tq, tk, tv;
+  const uint64_t cache_rows = static_cast<uint64_t>(a.num_blocks) * a.block_size;
+  if (!make_map(&tq, a.q, a.total_q, a.num_q_heads, kTile) ||
+      !make_map(&tk, a.k_cache, cache_rows, a.num_kv_heads, box_rows) ||
+      !make_map(&tv, a.v_cache, cache_rows, a.num_kv_heads, box_rows))
+    return cudaErrorInvalidValue;
+  PPParams p;
+  p.out = static_cast<__nv_bfloat16 *>(a.out);
+  p.cu_q = a.cu_seqlens_q;
+  p.cu_k = a.cu_seqlens_k;
+  p.block_tables = a.block_tables;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
+  p.total_q = a.total_q;
+  p.num_q_heads = a.num_q_heads;
+  p.group = a.num_q_heads / a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.num_blocks = a.num_blocks;
+  p.max_seqlen_q = a.max_seqlen_q;
+  p.max_seqlen_k = a.max_seqlen_k;
+  p.causal = a.causal ? 1 : 0;
+  p.box_rows = box_rows;
+  p.scale_log2 = a.scale * kLog2e;
+  p.err = a.err;
+  dim3 grid((a.max_seqlen_q + kTile - 1) / kTile, a.num_q_heads / 2, a.num_seqs);
+  prefill_pp_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv
