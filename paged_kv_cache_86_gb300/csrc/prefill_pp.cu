@@ -41,17 +41,18 @@ constexpr int kTile = 128;
 constexpr int kHD = 128;
 constexpr int kRegion = 16384;
 constexpr int kTileBytes = 2 * kRegion;
-constexpr int kStages = 2;
-constexpr int kThreads = 320;        // TMA, MMA, softmax A (4 warps), softmax B (4 warps)
+constexpr int kKStages = 3;          // K is needed first (S), so it runs furthest ahead
+constexpr int kVStages = 2;
+constexpr int kThreads = 352;        // K/Q TMA, MMA, softmax A (4 warps), softmax B (4 warps), V TMA
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.f;
 
 constexpr int kOffQ = 0;                              // Q_A, Q_B
 constexpr int kOffK = kOffQ + 2 * kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
-constexpr int kNumBars = 1 + 4 * kStages + 6;         // q, k/v full/empty, s_full x2, p_full x2, pv_done x2
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 6;  // q, k full/empty, v full/empty, s/p/pv x2
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
 
 struct PPParams {
@@ -146,22 +147,25 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   const uint32_t bar0 = base + kOffBar;
   const uint32_t q_full = bar0;
+  constexpr int kB = 1 + 2 * kKStages + 2 * kVStages;
   auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto v_full = [&](int s) { return bar0 + 8u * (1 + kStages + s); };
-  auto k_empty = [&](int s) { return bar0 + 8u * (1 + 2 * kStages + s); };
-  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 3 * kStages + s); };
-  auto s_full = [&](int x) { return bar0 + 8u * (1 + 4 * kStages + x); };
-  auto p_full = [&](int x) { return bar0 + 8u * (3 + 4 * kStages + x); };
-  auto pv_done = [&](int x) { return bar0 + 8u * (5 + 4 * kStages + x); };
+  auto k_empty = [&](int s) { return bar0 + 8u * (1 + kKStages + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * kKStages + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * kKStages + kVStages + s); };
+  auto s_full = [&](int x) { return bar0 + 8u * (kB + x); };
+  auto p_full = [&](int x) { return bar0 + 8u * (kB + 2 + x); };
+  auto pv_done = [&](int x) { return bar0 + 8u * (kB + 4 + x); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + kNumBars * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(k_full(s), 1);
-      mbar_init(v_full(s), 1);
       mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -190,19 +194,25 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     raise_error(p.err, PKV_DEVERR_TIMEOUT);
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------- producer
-    int k_issued = 0, v_issued = 0;
+  if (warp == 0 || warp == 10) {
+    // ------------------------------------------------------------ producers
+    // warp 0 loads Q_A, Q_B and the K tiles, warp 10 the V tiles
+    const bool is_k = warp == 0;
+    const int stages = is_k ? kKStages : kVStages;
+    int issued = 0;
     bool ok = true;
     if (n_tiles > 0) {
       if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
-        for (int x = 0; x < 2; ++x) {
-          tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, qh_a + x, q_begin + r0, q_full);
-          tma_load_3d(sQ + x * kTileBytes + kRegion, &tm_q, 64, qh_a + x, q_begin + r0, q_full);
+        if (is_k) {
+          tma_prefetch_desc(&tm_q);
+          tma_prefetch_desc(&tm_k);
+          mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+          for (int x = 0; x < 2; ++x) {
+            tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, qh_a + x, q_begin + r0, q_full);
+            tma_load_3d(sQ + x * kTileBytes + kRegion, &tm_q, 64, qh_a + x, q_begin + r0, q_full);
+          }
+        } else {
+          tma_prefetch_desc(&tm_v);
         }
       }
       const int R = p.box_rows;
@@ -210,49 +220,45 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const int oob_row = p.num_blocks * p.block_size;
       const int32_t *bt = p.block_tables + static_cast<size_t>(seq) * p.max_blocks_per_seq;
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j % kStages;
-        const int round = j / kStages;
+        const int s = j % stages;
+        const int round = j / stages;
         int row = oob_row;
         if (lane < pieces) {
           const int key = j * kTile + lane * R;
           if (key < k_len) {
             const int blk = __ldg(bt + key / p.block_size);
             if (blk >= 0 && blk < p.num_blocks) row = blk * p.block_size + key % p.block_size;
-            else raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+            else if (is_k) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
           }
         }
-        for (int which = 0; which < 2 && ok; ++which) {
-          const uint32_t full = which ? v_full(s) : k_full(s);
-          const uint32_t empty = which ? v_empty(s) : k_empty(s);
-          const uint32_t dst = which ? sV(s) : sK(s);
-          const CUtensorMap *map = which ? &tm_v : &tm_k;
-          int good = 1;
-          if (lane == 0) {
-            if (round > 0 && !mbar_wait(empty, (round - 1) & 1, abort_flag)) {
-              good = 0;
-              fail();
-            } else {
-              mbar_arrive_expect_tx(full, kTileBytes);
-            }
+        const uint32_t full = is_k ? k_full(s) : v_full(s);
+        const uint32_t empty = is_k ? k_empty(s) : v_empty(s);
+        const uint32_t dst = is_k ? sK(s) : sV(s);
+        const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+        int good = 1;
+        if (lane == 0) {
+          if (round > 0 && !mbar_wait(empty, (round - 1) & 1, abort_flag)) {
+            good = 0;
+            fail();
+          } else {
+            mbar_arrive_expect_tx(full, kTileBytes);
           }
-          good = __shfl_sync(0xffffffffu, good, 0);
-          if (!good) {
-            ok = false;
-            break;
-          }
-          if (lane < pieces) {
-            tma_load_3d(dst + lane * R * 128, map, 0, kvh, row, full);
-            tma_load_3d(dst + kRegion + lane * R * 128, map, 64, kvh, row, full);
-          }
-          if (which) ++v_issued; else ++k_issued;
         }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        if (lane < pieces) {
+          tma_load_3d(dst + lane * R * 128, map, 0, kvh, row, full);
+          tma_load_3d(dst + kRegion + lane * R * 128, map, 64, kvh, row, full);
+        }
+        ++issued;
       }
       if (lane == 0) {  // drain: the last copies must land before the CTA exits
-        mbar_wait(q_full, 0, nullptr);
-        for (int j = max(0, k_issued - kStages); j < k_issued; ++j)
-          mbar_wait(k_full(j % kStages), (j / kStages) & 1, nullptr);
-        for (int j = max(0, v_issued - kStages); j < v_issued; ++j)
-          mbar_wait(v_full(j % kStages), (j / kStages) & 1, nullptr);
+        if (is_k) mbar_wait(q_full, 0, nullptr);
+        for (int j = max(0, issued - stages); j < issued; ++j)
+          mbar_wait(is_k ? k_full(j % stages) : v_full(j % stages), (j / stages) & 1, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -263,7 +269,7 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       bool ok = mbar_wait(q_full, 0, abort_flag);
       int s_commits[2] = {0, 0}, pv_commits[2] = {0, 0};
       auto issue_s = [&](int x, int j) {
-        const int s = j % kStages;
+        const int s = j % kKStages;
         const uint32_t q = sQ + x * kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk)
@@ -273,7 +279,7 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (x == 1) umma_commit(k_empty(s));   // K(j) has fed both heads
       };
       auto issue_pv = [&](int x, int j) -> bool {
-        const int s = j % kStages;
+        const int s = j % kVStages;
         if (!mbar_wait(p_full(x), j & 1, abort_flag)) return false;
         tc_fence_after();
 #pragma unroll
@@ -293,14 +299,14 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         issue_s(1, 0);
       }
       for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j % kStages;
-        if (!mbar_wait(v_full(s), (j / kStages) & 1, abort_flag)) { ok = false; break; }
+        const int sv = j % kVStages;
+        if (!mbar_wait(v_full(sv), (j / kVStages) & 1, abort_flag)) { ok = false; break; }
         const bool more = j + 1 < n_tiles;
-        const int s1 = (j + 1) % kStages;
+        const int s1 = (j + 1) % kKStages;
         for (int x = 0; ok && x < 2; ++x) {
           if (!issue_pv(x, j)) { ok = false; break; }
           if (more) {
-            if (x == 0 && !mbar_wait(k_full(s1), ((j + 1) / kStages) & 1, abort_flag)) { ok = false; break; }
+            if (x == 0 && !mbar_wait(k_full(s1), ((j + 1) / kKStages) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
             issue_s(x, j + 1);
           }
