@@ -58,6 +58,36 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   return *reinterpret_cast<float2 *>(&rd);
 }
 
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  unsigned long long ra, rb, rd;
+  ra = *reinterpret_cast<unsigned long long *>(&a);
+  rb = *reinterpret_cast<unsigned long long *>(&b);
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  return *reinterpret_cast<float2 *>(&rd);
+}
+
+// max(a, b, c) in one instruction (three-operand max.f32, sm_100+); like
+// fmaxf, a NaN operand is ignored.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of 128 values as eight independent chains of three-operand maxima
+// (68 instructions, dependency depth 10) instead of one serial chain of 127.
+__device__ __forceinline__ float max128(const float (&v)[128]) {
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = fmaxf(v[i], v[i + 8]);
+#pragma unroll
+  for (int e = 16; e < 128; e += 16) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = fmax3(acc[i], v[e + i], v[e + 8 + i]);
+  }
+  return fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
+}
+
 // ------------------------------------------------------------ shared mem --
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

@@ -341,17 +341,11 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tmem_wait_ld();
 
       const int key0 = j * kTile;
-      float mt = -INFINITY;
-      if (key0 + kTile <= visible) {
+      if (key0 + kTile > visible) {
 #pragma unroll
-        for (int e = 0; e < kTile; ++e) mt = fmaxf(mt, s[e]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < kTile; ++e) {
-          s[e] = (key0 + e < visible) ? s[e] : -INFINITY;
-          mt = fmaxf(mt, s[e]);
-        }
+        for (int e = 0; e < kTile; ++e) s[e] = (key0 + e < visible) ? s[e] : -INFINITY;
       }
+      const float mt = max128(s);
       // lazy rescale: only when the maximum grows by more than 2^8 after scaling
       const bool grow = mt != -INFINITY && (m_used == -INFINITY || (mt - m_used) * c > kRescaleThreshold);
       float alpha = 1.f;
@@ -376,22 +370,27 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         tmem_wait_st();
       }
-      // P = exp2(s*c - m*c) as bf16 pairs over TMEM columns 0..63 of S_X
+      // P = exp2(s*c - m*c) as bf16 pairs over TMEM columns 0..63 of S_X; the
+      // scaling and the row sum run two lanes per instruction (FFMA2 / FADD2).
       const float mc = m_used * c;
-      float rs = 0.f;
+      float2 rs2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) rs2[i] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float a0 = ex2(fmaf(s[half * 64 + 2 * e], c, -mc));
-          const float a1 = ex2(fmaf(s[half * 64 + 2 * e + 1], c, -mc));
-          rs += a0 + a1;
-          pk[e] = float2_to_bf16x2(a0, a1);
+          const float2 xx = ffma2(make_float2(s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]),
+                                  make_float2(c, c), make_float2(-mc, -mc));
+          const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+          rs2[e & 3] = fadd2(rs2[e & 3], pp);
+          pk[e] = float2_to_bf16x2(pp.x, pp.y);
         }
         tmem_st32_u(tmem_s(x) + lane_off + half * 32, pk);
       }
-      l_sum += rs;
+      const float2 rs01 = fadd2(rs2[0], rs2[1]), rs23 = fadd2(rs2[2], rs2[3]);
+      l_sum += (rs01.x + rs01.y) + (rs23.x + rs23.y);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
