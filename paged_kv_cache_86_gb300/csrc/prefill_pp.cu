@@ -9,8 +9,11 @@
 //
 //   * One CTA = one 128-row query tile of TWO query heads A and B of the same
 //     KV head (GQA): the K and V tiles are loaded once for both.
-//   * Two softmax warpgroups (warps 2-5 for A, 6-9 for B). While one computes
+//   * Two softmax warpgroups (warps 0-3 for A, 4-7 for B). While one computes
 //     the softmax of its tile, the tensor core runs the other head's S and PV.
+//     The third warpgroup holds the Q/K loader (warp 8), the MMA issuer (warp
+//     9) and the V loader (warp 10); it gives up most of its registers
+//     (setmaxnreg) so each softmax thread can keep a whole 128-score row live.
 //     MMA issue order per KV tile j: PV_A(j-1), S_A(j), PV_B(j-1), S_B(j).
 //   * All four accumulators live in TMEM (S_A, S_B, O_A, O_B: 4 x 128 columns,
 //     the whole TMEM of the SM). P is written back as bf16 over the first 64
@@ -43,7 +46,14 @@ constexpr int kRegion = 16384;
 constexpr int kTileBytes = 2 * kRegion;
 constexpr int kKStages = 3;          // K is needed first (S), so it runs furthest ahead
 constexpr int kVStages = 2;
-constexpr int kThreads = 352;        // K/Q TMA, MMA, softmax A (4 warps), softmax B (4 warps), V TMA
+constexpr int kThreads = 384;        // softmax A (warpgroup 0), softmax B (1), loaders + MMA (2)
+constexpr int kWarpQK = 8, kWarpMma = 9, kWarpV = 10;
+// Register split: launched at 168 per thread (384 x 168 = 64512); warpgroup 2
+// drops to 88 and the two softmax warpgroups rise to 208, which adds back up
+// to the launch total: 2 x 128 x 208 + 128 x 88 = 64512.
+constexpr int kRegsLaunch = 168, kRegsLow = 88, kRegsHigh = 208;
+static_assert(2 * 128 * kRegsHigh + 128 * kRegsLow == kThreads * kRegsLaunch,
+              "setmaxnreg split must add up to the launch allocation");
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.f;
@@ -176,7 +186,7 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -194,134 +204,141 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     raise_error(p.err, PKV_DEVERR_TIMEOUT);
   };
 
-  if (warp == 0 || warp == 10) {
-    // ------------------------------------------------------------ producers
-    // warp 0 loads Q_A, Q_B and the K tiles, warp 10 the V tiles
-    const bool is_k = warp == 0;
-    const int stages = is_k ? kKStages : kVStages;
-    int issued = 0;
-    bool ok = true;
-    if (n_tiles > 0) {
-      if (lane == 0) {
-        if (is_k) {
-          tma_prefetch_desc(&tm_q);
-          tma_prefetch_desc(&tm_k);
-          mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
-          for (int x = 0; x < 2; ++x) {
-            tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, qh_a + x, q_begin + r0, q_full);
-            tma_load_3d(sQ + x * kTileBytes + kRegion, &tm_q, 64, qh_a + x, q_begin + r0, q_full);
-          }
-        } else {
-          tma_prefetch_desc(&tm_v);
-        }
-      }
-      const int R = p.box_rows;
-      const int pieces = kTile / R;
-      const int oob_row = p.num_blocks * p.block_size;
-      const int32_t *bt = p.block_tables + static_cast<size_t>(seq) * p.max_blocks_per_seq;
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j % stages;
-        const int round = j / stages;
-        int row = oob_row;
-        if (lane < pieces) {
-          const int key = j * kTile + lane * R;
-          if (key < k_len) {
-            const int blk = __ldg(bt + key / p.block_size);
-            if (blk >= 0 && blk < p.num_blocks) row = blk * p.block_size + key % p.block_size;
-            else if (is_k) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
-          }
-        }
-        const uint32_t full = is_k ? k_full(s) : v_full(s);
-        const uint32_t empty = is_k ? k_empty(s) : v_empty(s);
-        const uint32_t dst = is_k ? sK(s) : sV(s);
-        const CUtensorMap *map = is_k ? &tm_k : &tm_v;
-        int good = 1;
+  if (warp >= 8) {
+    // The loader / MMA warpgroup hands registers to the softmax warpgroups;
+    // each branch of the split holds exactly one setmaxnreg, executed by all
+    // four warps of its warpgroup.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsLow));
+    if (warp == kWarpQK || warp == kWarpV) {
+      // ------------------------------------------------------------ producers
+      // one warp loads Q_A, Q_B and the K tiles, the other the V tiles
+      const bool is_k = warp == kWarpQK;
+      const int stages = is_k ? kKStages : kVStages;
+      int issued = 0;
+      bool ok = true;
+      if (n_tiles > 0) {
         if (lane == 0) {
-          if (round > 0 && !mbar_wait(empty, (round - 1) & 1, abort_flag)) {
-            good = 0;
-            fail();
+          if (is_k) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+            for (int x = 0; x < 2; ++x) {
+              tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, qh_a + x, q_begin + r0, q_full);
+              tma_load_3d(sQ + x * kTileBytes + kRegion, &tm_q, 64, qh_a + x, q_begin + r0, q_full);
+            }
           } else {
-            mbar_arrive_expect_tx(full, kTileBytes);
+            tma_prefetch_desc(&tm_v);
           }
         }
-        good = __shfl_sync(0xffffffffu, good, 0);
-        if (!good) {
-          ok = false;
-          break;
+        const int R = p.box_rows;
+        const int pieces = kTile / R;
+        const int oob_row = p.num_blocks * p.block_size;
+        const int32_t *bt = p.block_tables + static_cast<size_t>(seq) * p.max_blocks_per_seq;
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          const int s = j % stages;
+          const int round = j / stages;
+          int row = oob_row;
+          if (lane < pieces) {
+            const int key = j * kTile + lane * R;
+            if (key < k_len) {
+              const int blk = __ldg(bt + key / p.block_size);
+              if (blk >= 0 && blk < p.num_blocks) row = blk * p.block_size + key % p.block_size;
+              else if (is_k) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+            }
+          }
+          const uint32_t full = is_k ? k_full(s) : v_full(s);
+          const uint32_t empty = is_k ? k_empty(s) : v_empty(s);
+          const uint32_t dst = is_k ? sK(s) : sV(s);
+          const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+          int good = 1;
+          if (lane == 0) {
+            if (round > 0 && !mbar_wait(empty, (round - 1) & 1, abort_flag)) {
+              good = 0;
+              fail();
+            } else {
+              mbar_arrive_expect_tx(full, kTileBytes);
+            }
+          }
+          good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) {
+            ok = false;
+            break;
+          }
+          if (lane < pieces) {
+            tma_load_3d(dst + lane * R * 128, map, 0, kvh, row, full);
+            tma_load_3d(dst + kRegion + lane * R * 128, map, 64, kvh, row, full);
+          }
+          ++issued;
         }
-        if (lane < pieces) {
-          tma_load_3d(dst + lane * R * 128, map, 0, kvh, row, full);
-          tma_load_3d(dst + kRegion + lane * R * 128, map, 64, kvh, row, full);
+        if (lane == 0) {  // drain: the last copies must land before the CTA exits
+          if (is_k) mbar_wait(q_full, 0, nullptr);
+          for (int j = max(0, issued - stages); j < issued; ++j)
+            mbar_wait(is_k ? k_full(j % stages) : v_full(j % stages), (j / stages) & 1, nullptr);
         }
-        ++issued;
       }
-      if (lane == 0) {  // drain: the last copies must land before the CTA exits
-        if (is_k) mbar_wait(q_full, 0, nullptr);
-        for (int j = max(0, issued - stages); j < issued; ++j)
-          mbar_wait(is_k ? k_full(j % stages) : v_full(j % stages), (j / stages) & 1, nullptr);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
-      constexpr uint32_t idesc_s = umma_idesc_bf16(kTile, kTile, false);
-      constexpr uint32_t idesc_pv = umma_idesc_bf16(kTile, kHD, true);  // B (V) MN-major
-      bool ok = mbar_wait(q_full, 0, abort_flag);
-      int s_commits[2] = {0, 0}, pv_commits[2] = {0, 0};
-      auto issue_s = [&](int x, int j) {
-        const int s = j % kKStages;
-        const uint32_t q = sQ + x * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kHD / 16; ++kk)
-          umma_bf16(tmem_s(x), desc_kmajor(q, kk), desc_kmajor(sK(s), kk), idesc_s, kk > 0 ? 1u : 0u);
-        umma_commit(s_full(x));
-        ++s_commits[x];
-        if (x == 1) umma_commit(k_empty(s));   // K(j) has fed both heads
-      };
-      auto issue_pv = [&](int x, int j) -> bool {
-        const int s = j % kVStages;
-        if (!mbar_wait(p_full(x), j & 1, abort_flag)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_tmem_a(tmem_o(x), tmem_s(x) + kk * 8, desc_v_mnmajor(sV(s), kk), idesc_pv,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(pv_done(x));
-        ++pv_commits[x];
-        if (x == 1) umma_commit(v_empty(s));   // V(j) has fed both heads
-        return true;
-      };
-      // S_A(0), S_B(0), then per tile: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
-      if (ok) ok = mbar_wait(k_full(0), 0, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int sv = j % kVStages;
-        if (!mbar_wait(v_full(sv), (j / kVStages) & 1, abort_flag)) { ok = false; break; }
-        const bool more = j + 1 < n_tiles;
-        const int s1 = (j + 1) % kKStages;
-        for (int x = 0; ok && x < 2; ++x) {
-          if (!issue_pv(x, j)) { ok = false; break; }
-          if (more) {
-            if (x == 0 && !mbar_wait(k_full(s1), ((j + 1) / kKStages) & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            issue_s(x, j + 1);
+    } else if (warp == kWarpMma) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0 && n_tiles > 0) {
+        constexpr uint32_t idesc_s = umma_idesc_bf16(kTile, kTile, false);
+        constexpr uint32_t idesc_pv = umma_idesc_bf16(kTile, kHD, true);  // B (V) MN-major
+        bool ok = mbar_wait(q_full, 0, abort_flag);
+        int s_commits[2] = {0, 0}, pv_commits[2] = {0, 0};
+        auto issue_s = [&](int x, int j) {
+          const int s = j % kKStages;
+          const uint32_t q = sQ + x * kTileBytes;
+  #pragma unroll
+          for (int kk = 0; kk < kHD / 16; ++kk)
+            umma_bf16(tmem_s(x), desc_kmajor(q, kk), desc_kmajor(sK(s), kk), idesc_s, kk > 0 ? 1u : 0u);
+          umma_commit(s_full(x));
+          ++s_commits[x];
+          if (x == 1) umma_commit(k_empty(s));   // K(j) has fed both heads
+        };
+        auto issue_pv = [&](int x, int j) -> bool {
+          const int s = j % kVStages;
+          if (!mbar_wait(p_full(x), j & 1, abort_flag)) return false;
+          tc_fence_after();
+  #pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_bf16_tmem_a(tmem_o(x), tmem_s(x) + kk * 8, desc_v_mnmajor(sV(s), kk), idesc_pv,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(pv_done(x));
+          ++pv_commits[x];
+          if (x == 1) umma_commit(v_empty(s));   // V(j) has fed both heads
+          return true;
+        };
+        // S_A(0), S_B(0), then per tile: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+        if (ok) ok = mbar_wait(k_full(0), 0, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0);
+          issue_s(1, 0);
+        }
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          const int sv = j % kVStages;
+          if (!mbar_wait(v_full(sv), (j / kVStages) & 1, abort_flag)) { ok = false; break; }
+          const bool more = j + 1 < n_tiles;
+          const int s1 = (j + 1) % kKStages;
+          for (int x = 0; ok && x < 2; ++x) {
+            if (!issue_pv(x, j)) { ok = false; break; }
+            if (more) {
+              if (x == 0 && !mbar_wait(k_full(s1), ((j + 1) / kKStages) & 1, abort_flag)) { ok = false; break; }
+              tc_fence_after();
+              issue_s(x, j + 1);
+            }
           }
         }
+        if (!ok) fail();
+        for (int x = 0; x < 2; ++x) {  // every issued MMA completes before TMEM is freed
+          if (s_commits[x] > 0) mbar_wait(s_full(x), (s_commits[x] - 1) & 1, nullptr);
+          if (pv_commits[x] > 0) mbar_wait(pv_done(x), (pv_commits[x] - 1) & 1, nullptr);
+        }
       }
-      if (!ok) fail();
-      for (int x = 0; x < 2; ++x) {  // every issued MMA completes before TMEM is freed
-        if (s_commits[x] > 0) mbar_wait(s_full(x), (s_commits[x] - 1) & 1, nullptr);
-        if (pv_commits[x] > 0) mbar_wait(pv_done(x), (pv_commits[x] - 1) & 1, nullptr);
-      }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kRegsHigh));
     // ------------------------------------------------------- softmax A / B
-    const int x = (warp - 2) >> 2;                   // 0: head A, 1: head B
+    const int x = warp >> 2;                         // 0: head A, 1: head B
     const int quad = warp & 3;                       // TMEM lanes 32*quad .. 32*quad+31
     const int r = quad * 32 + lane;                  // query row inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -436,7 +453,7 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -481,6 +498,12 @@ cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
   std::call_once(attr_once, [] {
     attr_err = cudaFuncSetAttribute(prefill_pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kSmemBytes);
+    // setmaxnreg.inc waits until the registers it asks for are free; the split
+    // only adds up if the kernel was built with exactly kRegsLaunch per thread,
+    // so refuse to launch any other build rather than risk a wait that never ends.
+    cudaFuncAttributes fa;
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_pp_kernel);
+    if (attr_err == cudaSuccess && fa.numRegs != kRegsLaunch) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return attr_err;
   int box_rows = a.block_size & -a.block_size;
