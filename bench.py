@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -144,6 +145,22 @@ def make_workload(name, seed_offset=0, fill="device", num_seqs=None):
     return fn(**kw)
 
 
+def max_over_ranks(x, world, device):
+    """The slowest rank's value (the job's time); a no-op on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, units_per_rank, ms):
+    """Whole-job units per second: every rank processed units_per_rank in ms."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def decode_bytes(w) -> int:
     """Algorithmic HBM bytes of one decode launch: K and V of every cached token
     once per KV head, q in, out, block-table entries and context lengths."""
@@ -159,10 +176,15 @@ def store_bytes(w) -> int:
 
 
 def source_hash(paths):
+    """Hash of the code of the given sources with comments and blank space
+    stripped, so that editing a comment does not orphan a recorded profile."""
     m = hashlib.sha256()
     for p in paths:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            m.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        m.update(" ".join(text.split()).encode())
     return m.hexdigest()[:16]
 
 
@@ -277,9 +299,9 @@ def run_pkv(args, rank, world, device):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        step_ms = e0.elapsed_time(e1) / args.steps
+        step_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
         if args.quick:
-            return {"metric": METRIC, "value": world * w.num_seqs / (step_ms * 1e-3), "unit": UNIT,
+            return {"metric": METRIC, "value": job_throughput(world, w.num_seqs, step_ms), "unit": UNIT,
                     "n_gpus": world, "steps": args.steps, "ms_per_step": step_ms,
                     "config": {"workload": w.name, "num_seqs": w.num_seqs}, "quick": True}
 
@@ -299,10 +321,6 @@ def run_pkv(args, rank, world, device):
     if pkv.get_device_errors() != 0:
         raise RuntimeError("device-side range check fired during the timed region")
 
-    if world > 1:
-        tt = torch.tensor([step_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        step_ms = float(tt.item())
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs from pinned memory, store + decode, D2H of the output
@@ -335,16 +353,13 @@ def run_pkv(args, rank, world, device):
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b) / args.steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
 
     peak, peak_kind = measured_peaks()
     dbytes = decode_bytes(w)
     achieved = dbytes / (decode_ms * 1e-3) / 1e9
     result = {
-        "metric": METRIC, "value": world * w.num_seqs / (step_ms * 1e-3), "unit": UNIT,
+        "metric": METRIC, "value": job_throughput(world, w.num_seqs, step_ms), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, recipe in DESIGN.md)",
@@ -364,7 +379,7 @@ def run_pkv(args, rank, world, device):
                      "algorithmic_bytes_per_launch": dbytes, "launch_ms": decode_ms},
         "ops": {"store_ms": store_ms, "store_gbs": store_bytes(w) / (store_ms * 1e-3) / 1e9,
                 "decode_ms": decode_ms},
-        "e2e": {"value": world * w.num_seqs / (e2e_ms * 1e-3), "unit": UNIT,
+        "e2e": {"value": job_throughput(world, w.num_seqs, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * 4,
         "clocks": clocks.summary(),
@@ -410,19 +425,28 @@ def measure_prefill(args, device, steps):
         store()
         prefill()
     torch.cuda.synchronize()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # > L2 between launches
+    # L2 (129 MB) is flushed before every timed launch by writing 256 MiB and
+    # then reading 256 MiB, so the launch starts with clean, unrelated lines: a
+    # write-only flush leaves ~129 MB of dirty lines whose write-back would be
+    # charged to the next kernel. The store is also timed after the write-only
+    # flush and reported beside it.
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush_rd = torch.ones(64 << 20, dtype=torch.float32, device=device)
     res = {}
-    for name, fn in (("store", store), ("prefill", prefill)):
+    for name, fn, clean in (("store", store, True), ("prefill", prefill, True),
+                            ("store_dirty_l2", store, False)):
         times = []
         for _ in range(steps):
             flush.zero_()
+            if clean:
+                flush_rd.sum()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
             b.record(stream)
             torch.cuda.synchronize()
             times.append(a.elapsed_time(b))
-        res[name] = statistics.mean(times)
+        res[name] = statistics.median(times)
     if pkv.get_device_errors() != 0:
         raise RuntimeError("device-side range check fired in the prefill measurement")
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
@@ -431,9 +455,12 @@ def measure_prefill(args, device, steps):
     hpeak, _ = measured_peaks()
     fl = prefill_flops(w)
     sb = store_bytes(w)
-    return {"workload": w.name, "l2": "256 MiB buffer written between launches",
+    return {"workload": w.name,
+            "l2": "256 MiB written then 256 MiB read before each launch (clean L2); median of launches",
             "store_ms": res["store"], "store_gbs": sb / (res["store"] * 1e-3) / 1e9,
             "store_frac_of_hbm": sb / (res["store"] * 1e-3) / 1e9 / hpeak,
+            "store_ms_after_write_only_flush": res["store_dirty_l2"],
+            "store_frac_of_hbm_after_write_only_flush": sb / (res["store_dirty_l2"] * 1e-3) / 1e9 / hpeak,
             "prefill_ms": res["prefill"], "prefill_tflops": fl / (res["prefill"] * 1e-3) / 1e12,
             "prefill_frac_of_bf16": fl / (res["prefill"] * 1e-3) / 1e12 / tpeak,
             "prefill_flops": fl, "peak_bf16_tflops": tpeak, "peak_source": "measured bf16_tflops (burst)"}

@@ -20,9 +20,10 @@
 //     P^T is block-diagonal: row h*T + t holds p only in the columns of head h,
 //     so each query head accumulates only the V rows of its own KV head.
 //
-// Per CTA (192 threads, one CTA per SM): warp 0 is the TMA producer (Q rows of a
-// sequence when a segment starts, then K and V boxes per stage, three stages of
-// 64 KB), warp 1 owns TMEM and issues the MMAs, warps 2-5 run the softmax with
+// Per CTA (224 threads, one CTA per SM): warp 0 loads Q rows when a sequence
+// segment starts and the K box of every stage, warp 6 the V box (separate K and
+// V rings of up to three 32 KB stages each, so V never holds up the next S),
+// warp 1 owns TMEM and issues the MMAs, warps 2-5 run the softmax with
 // one thread per row: the T rows of a KV head sit in one warp, so the per-head
 // stage maximum and the row sums are warp shuffles. The running maximum is
 // rescaled lazily (only when it grows by more than 2^8), and the rare rescale of
