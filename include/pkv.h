@@ -10,7 +10,9 @@
  *   pkv_store_kvcache  write each new token's K and V into the cache slot
  *                      named by slot_mapping;
  *   pkv_paged_decode   one query per sequence over its context_lens[i] cached
- *                      tokens, found through its block_tables row;
+ *                      tokens, found through its block_tables row
+ *                      (pkv_decode_step: the store of each sequence's newest
+ *                      token and the decode in one call);
  *   pkv_paged_prefill  varlen query chunks (cu_seqlens_q) over their cached
  *                      prefix plus themselves (cu_seqlens_k), causal.
  *
@@ -115,8 +117,11 @@ pkv_status pkv_store_kvcache(const void *key, const void *value,
  *                     num_kv_heads, head_dim) bytes, 256-byte aligned. Its
  *                     contents need no initialisation and are scratch after
  *                     the call; two calls in flight at once need two workspaces.
- *   Supported: head_dim 128; num_kv_heads in {1, 2, 4, 8}; num_q_heads /
- *   num_kv_heads in {1, 2, 4, 8}; any block_size >= 1; any scale.
+ *   Supported: head_dim 128, num_q_heads a multiple of num_kv_heads, any
+ *   scale, and either block_size a multiple of 8 with at most 16 query heads
+ *   per KV head (tensor-core kernels), or any block_size >= 1 with
+ *   num_kv_heads in {1, 2, 4, 8} and num_q_heads / num_kv_heads in {1, 2, 4,
+ *   8}. Other shapes return PKV_ERR_SHAPE.
  * The work is split into equal token ranges over the GPU's SMs; a sequence that
  * spans several ranges is finished by a log-sum-exp combine pass.
  */
@@ -132,6 +137,42 @@ pkv_status pkv_paged_decode(void *out, const void *q,
                             int32_t block_size, int32_t num_blocks, float scale,
                             void *workspace, size_t workspace_bytes,
                             pkv_dtype dtype, void *stream);
+
+/* ----------------------------------------------------------- decode step --
+ * pkv_decode_step: one decode step of a batch in one call -- the store of each
+ * sequence's newest token followed by pkv_paged_decode, with the same
+ * arguments, supported shapes, workspace and errors as pkv_paged_decode, plus:
+ *   key_new, value_new  [num_seqs, num_kv_heads, head_dim] bf16 rows (token
+ *                       strides key_token_stride / value_token_stride in
+ *                       elements, multiples of 8, 16-byte aligned): the K and V
+ *                       of each sequence's newest token.
+ * Row i is written to the cache at logical position n_i - 1 of sequence i,
+ * n_i = context_lens[i] (which counts the new token), i.e. to slot
+ * block_tables[i][(n_i - 1) / block_size] * block_size + (n_i - 1) % block_size,
+ * the last filled row of the sequence's last block (nano vllm代码详解 §2
+ * Sequence: last_block_num_tokens; §3.2.4 may_append: the last block is the
+ * one being written), and then attended to. Sequences with n_i == 0 store nothing and get a zero
+ * row. The result equals pkv_store_kvcache with those slots followed by
+ * pkv_paged_decode; on the all-heads tensor-core kernel both happen in one
+ * decode launch (each CTA writes the new tokens whose positions it owns before
+ * its first load), otherwise a store launch runs first on the same stream.
+ * A block id outside [0, num_blocks) skips the write and sets
+ * PKV_DEVERR_BLOCK_ID.
+ * Graphs: the launches depend only on the host arguments, so a call can be
+ * captured in a CUDA graph and replayed with new contents in the same buffers;
+ * padding a batch up to a captured size with context_lens 0 rows is allowed.
+ */
+pkv_status pkv_decode_step(void *out, const void *q,
+                           const void *key_new, const void *value_new,
+                           int64_t key_token_stride, int64_t value_token_stride,
+                           void *k_cache, void *v_cache,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t num_seqs,
+                           int32_t max_context_len,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, float scale,
+                           void *workspace, size_t workspace_bytes,
+                           pkv_dtype dtype, void *stream);
 
 /* ------------------------------------------------- decode, no allocation --
  * pkv_paged_decode_static_ws: the same computation, arguments and errors as

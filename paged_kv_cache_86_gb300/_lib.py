@@ -57,6 +57,8 @@ def load(path: str = LIB_PATH):
         lib.pkv_decode_workspace_size.restype = sz
         lib.pkv_paged_decode.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
                                          i32, i32, f32, vp, sz, ctypes.c_int, vp]
+        lib.pkv_decode_step.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, i32, vp, i32, i32,
+                                        i32, i32, i32, i32, i32, f32, vp, sz, ctypes.c_int, vp]
         lib.pkv_prefill_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.pkv_prefill_workspace_size.restype = sz
         lib.pkv_paged_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, i32, i32,
@@ -66,8 +68,8 @@ def load(path: str = LIB_PATH):
         lib.pkv_status_string.argtypes = [ctypes.c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_version.restype = i32
-        for name in ("pkv_store_kvcache", "pkv_paged_decode", "pkv_paged_prefill",
-                     "pkv_get_device_errors"):
+        for name in ("pkv_store_kvcache", "pkv_paged_decode", "pkv_decode_step",
+                     "pkv_paged_prefill", "pkv_get_device_errors"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -166,6 +168,53 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                                 hq, hkv, d, bs, nb, float(scale), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), PKV_BF16,
                                 _stream(q, stream)), "pkv_paged_decode")
+    return out
+
+
+def decode_step(q, key_new, value_new, k_cache, v_cache, block_tables, context_lens,
+                scale: float, max_context_len: int | None = None, out=None, workspace=None,
+                stream=None) -> torch.Tensor:
+    """One decode step: writes each sequence's newest K/V row (key_new / value_new
+    [S, Hkv, D], token rows may be strided) at its last logical position
+    context_lens[i] - 1, then decodes; returns out [S, Hq, D] bf16."""
+    lib = load()
+    _need(q, "q", torch.bfloat16, 3)
+    for t, n in ((key_new, "key_new"), (value_new, "value_new")):
+        _need(t, n, torch.bfloat16, 3)
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{n} rows must be contiguous [Hkv, D] blocks")
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    if not (q.is_contiguous() and k_cache.is_contiguous() and v_cache.is_contiguous()
+            and block_tables.is_contiguous() and context_lens.is_contiguous()):
+        raise ValueError("decode tensors must be contiguous")
+    s, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("q / cache head_dim mismatch")
+    if key_new.shape != (s, hkv, d) or value_new.shape != (s, hkv, d):
+        raise ValueError("key_new / value_new must be [S, Hkv, D]")
+    if block_tables.shape[0] != s or context_lens.shape[0] != s:
+        raise ValueError("metadata rows must equal the number of sequences")
+    mb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = mb * bs
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
+    if out.shape != q.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like q")
+    need = decode_workspace_size(s, hq, hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(lib.pkv_decode_step(_ptr(out), _ptr(q), _ptr(key_new), _ptr(value_new),
+                               key_new.stride(0), value_new.stride(0), _ptr(k_cache),
+                               _ptr(v_cache), _ptr(block_tables), mb, _ptr(context_lens), s,
+                               int(max_context_len), hq, hkv, d, bs, nb, float(scale),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                               PKV_BF16, _stream(q, stream)), "pkv_decode_step")
     return out
 
 

@@ -96,13 +96,18 @@ size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t 
   return pkv::decode_workspace_upper_bound(num_seqs, num_q_heads, num_kv_heads, &e);
 }
 
-pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
-                            const int32_t *block_tables, int32_t max_blocks_per_seq,
-                            const int32_t *context_lens, int32_t num_seqs,
-                            int32_t max_context_len, int32_t num_q_heads, int32_t num_kv_heads,
-                            int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
-                            void *workspace, size_t workspace_bytes, pkv_dtype dtype,
-                            void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of pkv_paged_decode and pkv_decode_step (key_new == nullptr for the former).
+pkv_status decode_call(void *out, const void *q, const void *key_new, const void *value_new,
+                       int64_t key_stride, int64_t value_stride, const void *k_cache,
+                       const void *v_cache, const int32_t *block_tables,
+                       int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                       int32_t max_context_len, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                       void *workspace, size_t workspace_bytes, pkv_dtype dtype, void *stream) {
   if (dtype != PKV_BF16) return PKV_ERR_DTYPE;
   if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || block_size < 1 || num_blocks < 1 ||
       max_blocks_per_seq < 0 || max_context_len < 0 || !std::isfinite(scale))
@@ -116,6 +121,12 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
     return PKV_ERR_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_ARG;
+  if (key_new != nullptr || value_new != nullptr) {
+    const int64_t row = int64_t(num_kv_heads) * head_dim;
+    if (!key_new || !value_new || !aligned16(key_new) || !aligned16(value_new) ||
+        key_stride < row || value_stride < row || key_stride % 8 != 0 || value_stride % 8 != 0)
+      return PKV_ERR_ARG;
+  }
   cudaError_t e;
   pkv::DecodePlan plan;
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_SHAPE;
@@ -144,7 +155,42 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.err = err;
+  a.key_new = key_new;
+  a.value_new = value_new;
+  a.key_stride = key_stride;
+  a.value_stride = value_stride;
   return from_cuda(pkv::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *context_lens, int32_t num_seqs,
+                            int32_t max_context_len, int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                            void *workspace, size_t workspace_bytes, pkv_dtype dtype,
+                            void *stream) {
+  return decode_call(out, q, nullptr, nullptr, 0, 0, k_cache, v_cache, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_q_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, scale, workspace,
+                     workspace_bytes, dtype, stream);
+}
+
+pkv_status pkv_decode_step(void *out, const void *q, const void *key_new, const void *value_new,
+                           int64_t key_token_stride, int64_t value_token_stride, void *k_cache,
+                           void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                           const int32_t *context_lens, int32_t num_seqs, int32_t max_context_len,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, float scale, void *workspace,
+                           size_t workspace_bytes, pkv_dtype dtype, void *stream) {
+  if (num_seqs > 0 && (!key_new || !value_new)) return PKV_ERR_ARG;
+  return decode_call(out, q, key_new, value_new, key_token_stride, value_token_stride, k_cache,
+                     v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     max_context_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, workspace, workspace_bytes, dtype, stream);
 }
 
 size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,

@@ -671,6 +671,11 @@ bool choose_decode_plan(int num_q_heads, int num_kv_heads, int block_size, Decod
     plan->grid = decode_tc_grid();
     return plan->grid > 0;
   }
+  // the CUDA-core kernel spreads 8 consumer warps evenly over the KV heads and
+  // is instantiated for groups of 1, 2, 4 and 8 query heads
+  const int group = num_q_heads / num_kv_heads;
+  if (kConsumerWarps % num_kv_heads != 0 || (group != 1 && group != 2 && group != 4 && group != 8))
+    return false;
   plan->kind = 1;
   plan->tc = false;
   plan->grid = split_grid(num_q_heads, num_kv_heads, status);
@@ -716,6 +721,12 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
   cp.grid = grid;
   cp.group = group;
   cp.tc = plan.tc ? 1 : 0;
+
+  // Decode step: the tcgen05 all-heads kernel stores the new tokens itself;
+  // the other kernels get them from a store launch first (same stream order).
+  if (a.key_new != nullptr && plan.kind != 3 &&
+      (e = launch_store_new_tokens(a, stream)) != cudaSuccess)
+    return e;
 
   if (plan.kind == 3) {
     const WsLayout lay = ws_layout(a.num_seqs, a.num_q_heads, 1, grid);

@@ -40,7 +40,19 @@ struct DecodeArgs {
   void *workspace;
   size_t workspace_bytes;
   uint32_t *err;
+  // Decode step only (nullptr otherwise): the newest token of each sequence,
+  // [num_seqs, Hkv, 128] bf16 rows with these token strides in elements, is
+  // written to the cache at logical position min(context_len, max_context_len) - 1
+  // before it is attended to.
+  const void *key_new = nullptr;
+  const void *value_new = nullptr;
+  int64_t key_stride = 0;
+  int64_t value_stride = 0;
 };
+
+// Writes each sequence's newest K/V row (DecodeArgs::key_new / value_new) at
+// its last logical position, one warp per sequence.
+cudaError_t launch_store_new_tokens(const DecodeArgs &a, cudaStream_t stream);
 
 // Which decode kernel runs and on how many CTAs. Block sizes that are a
 // multiple of 8 (and at most 16 query heads per KV head) run the tcgen05

@@ -69,3 +69,22 @@ def test_host_validation_needs_no_gpu(lib):
                                  float("nan"), null, 0, 0, null) == -1
     assert lib.pkv_paged_prefill(null, null, null, null, null, null, 8, 8, null, 4, 1, 8, 8, 2,
                                  128, 16, 8, 0.1, 1, null, 0, 1, null) == -3
+
+
+def test_decode_step_host_validation_needs_no_gpu(lib):
+    vp, null = ctypes.c_void_p, ctypes.c_void_p(0)
+    a = vp(256)  # aligned dummy addresses: never dereferenced, checks fail first
+
+    def step(key_new, value_new, ks, vs, num_seqs=2, head_dim=128, dtype=0, scale=0.1):
+        return lib.pkv_decode_step(a, a, key_new, value_new, ks, vs, a, a, a, 4, a, num_seqs, 64,
+                                   8, 2, head_dim, 16, 8, scale, a, 1 << 20, dtype, null)
+
+    assert step(a, a, 256, 256, dtype=7) == -3          # dtype
+    assert step(null, a, 256, 256) == -1                # missing new-token rows
+    assert step(a, null, 256, 256) == -1
+    assert step(a, a, 256, 256, head_dim=64) == -2      # head_dim 64
+    assert step(vp(264), a, 256, 256) == -1             # misaligned key_new
+    assert step(a, a, 255, 256) == -1                   # stride not a multiple of 8
+    assert step(a, a, 128, 256) == -1                   # stride shorter than a row (2 x 128)
+    assert step(a, a, 256, 256, scale=float("inf")) == -1
+    assert step(null, null, 0, 0, num_seqs=0) == 0      # nothing to do

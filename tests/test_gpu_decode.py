@@ -178,3 +178,15 @@ def test_decode_full_size_all_rows_within_convex_hull():
     vmax = max(t["v_cache"].abs().max().item(), t["value"].abs().max().item())
     assert torch.isfinite(out.float()).all()
     assert out.float().abs().max().item() <= vmax * (1 + 1e-2)
+
+
+def test_decode_rejects_shapes_no_kernel_covers():
+    # block size not a multiple of 8 with 3 KV heads: neither tensor-core kernel
+    # applies and the CUDA-core kernel needs Hkv dividing 8 -> PKV_ERR_SHAPE
+    w = W.decode_workload("unsupported", [5, 9], 6, 3, 3, seed=17)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    m = device_meta(w)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], m["block_tables"], m["context_lens"],
+                         w.scale)
+    assert e.value.status == -2
