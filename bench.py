@@ -1,9 +1,11 @@
 #!/usr/bin/env python
 """Benchmark of one decode step over a block-paged KV cache on GB300.
 
-A step is the whole hot path for one batch: store the batch's new K/V tokens
-into the cache by slot_mapping (pkv_store_kvcache), then paged decode attention
-over every sequence's cached context (pkv_paged_decode: plan, split, combine).
+A step is the whole hot path for one batch: store each sequence's new K/V token
+into the cache, then paged decode attention over every sequence's cached
+context, both through one pkv_decode_step call (a plan launch that also writes
+the new tokens, the attention kernel, the combine). The two-call path (pkv_store_kvcache + pkv_paged_decode) is
+timed beside it for the breakdown.
 
 Default workload: 512 sequences, context lengths clip(rint(exp(ln 800 +
 N(0,1))), 16, 4096), 32 query / 8 KV heads, head_dim 128, block size 16, a
@@ -145,6 +147,12 @@ def make_workload(name, seed_offset=0, fill="device", num_seqs=None):
     return fn(**kw)
 
 
+def decode_step_launches(w) -> int:
+    """Kernels one pkv_decode_step launches: plan (which also writes the new
+    tokens), attention, combine."""
+    return 3
+
+
 def max_over_ranks(x, world, device):
     """The slowest rank's value (the job's time); a no-op on one rank."""
     if world <= 1:
@@ -272,10 +280,21 @@ def run_pkv(args, rank, world, device):
     ws = torch.empty(pkv.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads),
                      dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
+    # the step's new K/V rows indexed by sequence (the workload keeps one row per
+    # non-empty sequence, in order)
+    if w.num_new_tokens == w.num_seqs:
+        kn, vn = t["key"], t["value"]
+    else:
+        kn = torch.zeros((w.num_seqs,) + tuple(t["key"].shape[1:]), dtype=t["key"].dtype, device=device)
+        vn = torch.zeros_like(kn)
+        nz = torch.from_numpy(np.nonzero(w.context_lens > 0)[0]).to(device)
+        kn[nz] = t["key"]
+        vn[nz] = t["value"]
 
     def step():
-        pkv.store_kvcache(t["key"], t["value"], t["k_cache"], t["v_cache"], sm)
-        pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], bt, cl, w.scale, out=out, workspace=ws)
+        # one decode step: store of each sequence's new token + paged decode
+        pkv.decode_step(t["q"], kn, vn, t["k_cache"], t["v_cache"], bt, cl, w.scale, out=out,
+                        workspace=ws)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -305,10 +324,18 @@ def run_pkv(args, rank, world, device):
                     "n_gpus": world, "steps": args.steps, "ms_per_step": step_ms,
                     "config": {"workload": w.name, "num_seqs": w.num_seqs}, "quick": True}
 
-        # per-op durations over the same number of steps, events on the launching stream
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        for a, b, c in evs:
+        # per-call durations over the same number of steps, events on the launching
+        # stream: the decode step call (the roofline's launch), then the two-call
+        # path (store, paged decode) for the breakdown
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            a.record(stream)
+            step()
+            b.record(stream)
+        evs2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                 torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b, c in evs2:
             a.record(stream)
             pkv.store_kvcache(t["key"], t["value"], t["k_cache"], t["v_cache"], sm)
             b.record(stream)
@@ -316,16 +343,18 @@ def run_pkv(args, rank, world, device):
                              workspace=ws)
             c.record(stream)
         torch.cuda.synchronize()
-    store_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
-    decode_ms = statistics.mean(b.elapsed_time(c) for _, b, c in evs)
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    store_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs2)
+    decode_ms = statistics.mean(b.elapsed_time(c) for _, b, c in evs2)
     if pkv.get_device_errors() != 0:
         raise RuntimeError("device-side range check fired during the timed region")
 
 
     # end to end through the public API with host buffers: H2D of the step's
-    # inputs from pinned memory, store + decode, D2H of the output
-    host = {k: t[k].cpu().pin_memory() for k in ("q", "key", "value")}
-    host_meta = {"bt": bt.cpu().pin_memory(), "cl": cl.cpu().pin_memory(), "sm": sm.cpu().pin_memory()}
+    # inputs from pinned memory, the decode step, D2H of the output
+    host = {"q": t["q"].cpu().pin_memory(), "key": kn.cpu().pin_memory(),
+            "value": vn.cpu().pin_memory()}
+    host_meta = {"bt": bt.cpu().pin_memory(), "cl": cl.cpu().pin_memory()}
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     dev_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
     dev_meta = {k: torch.empty_like(v, device=device) for k, v in host_meta.items()}
@@ -337,9 +366,8 @@ def run_pkv(args, rank, world, device):
             dev_in[k].copy_(host[k], non_blocking=True)
         for k in host_meta:
             dev_meta[k].copy_(host_meta[k], non_blocking=True)
-        pkv.store_kvcache(dev_in["key"], dev_in["value"], t["k_cache"], t["v_cache"], dev_meta["sm"])
-        pkv.paged_decode(dev_in["q"], t["k_cache"], t["v_cache"], dev_meta["bt"], dev_meta["cl"],
-                         w.scale, out=out, workspace=ws)
+        pkv.decode_step(dev_in["q"], dev_in["key"], dev_in["value"], t["k_cache"], t["v_cache"],
+                        dev_meta["bt"], dev_meta["cl"], w.scale, out=out, workspace=ws)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -356,8 +384,8 @@ def run_pkv(args, rank, world, device):
     e2e_ms = max_over_ranks(e2e_ms, world, device)
 
     peak, peak_kind = measured_peaks()
-    dbytes = decode_bytes(w)
-    achieved = dbytes / (decode_ms * 1e-3) / 1e9
+    dbytes = decode_bytes(w) + store_bytes(w)
+    achieved = dbytes / (call_ms * 1e-3) / 1e9
     result = {
         "metric": METRIC, "value": job_throughput(world, w.num_seqs, step_ms), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
@@ -372,16 +400,18 @@ def run_pkv(args, rank, world, device):
                          f"({(w.context_lens.astype(np.int64) * w.num_kv_heads * w.head_dim * 4).sum() / 1e9:.2f} GB > 129 MB L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kv_gbs": achieved,
-        "roofline": {"bound": "hbm", "kernel": "pkv_paged_decode (plan + split + combine)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "pkv_decode_step (plan + new-token store, tcgen05 decode, combine)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "traffic": profiled_traffic(w.name),
-                     "algorithmic_bytes_per_launch": dbytes, "launch_ms": decode_ms},
-        "ops": {"store_ms": store_ms, "store_gbs": store_bytes(w) / (store_ms * 1e-3) / 1e9,
-                "decode_ms": decode_ms},
+                     "algorithmic_bytes_per_launch": dbytes, "launch_ms": call_ms},
+        "ops": {"decode_step_ms": call_ms, "store_ms": store_ms,
+                "store_gbs": store_bytes(w) / (store_ms * 1e-3) / 1e9, "decode_ms": decode_ms,
+                "decode_gbs": decode_bytes(w) / (decode_ms * 1e-3) / 1e9},
         "e2e": {"value": job_throughput(world, w.num_seqs, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * 4,
+        "gpu_launches": args.steps * decode_step_launches(w),
         "clocks": clocks.summary(),
     }
     result["prefill_row"] = measure_prefill(args, device, steps=max(5, min(args.steps, 20)))

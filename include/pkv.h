@@ -151,11 +151,11 @@ pkv_status pkv_paged_decode(void *out, const void *q,
  * block_tables[i][(n_i - 1) / block_size] * block_size + (n_i - 1) % block_size,
  * the last filled row of the sequence's last block (nano vllm代码详解 §2
  * Sequence: last_block_num_tokens; §3.2.4 may_append: the last block is the
- * one being written), and then attended to. Sequences with n_i == 0 store nothing and get a zero
- * row. The result equals pkv_store_kvcache with those slots followed by
- * pkv_paged_decode; on the all-heads tensor-core kernel both happen in one
- * decode launch (each CTA writes the new tokens whose positions it owns before
- * its first load), otherwise a store launch runs first on the same stream.
+ * one being written), and then attended to. Sequences with n_i == 0 store
+ * nothing and get a zero row. The result equals pkv_store_kvcache with those
+ * slots followed by pkv_paged_decode, in the same three launches as
+ * pkv_paged_decode alone: the rows are written by the decode's planning
+ * launch, beside the range planning.
  * A block id outside [0, num_blocks) skips the write and sets
  * PKV_DEVERR_BLOCK_ID.
  * Graphs: the launches depend only on the host arguments, so a call can be

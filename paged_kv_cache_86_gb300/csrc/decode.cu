@@ -96,13 +96,54 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // units_per_token: 1 when a CTA range covers tokens of all KV heads (split
 // kernel), num_kv_heads when it covers (KV head, token) pairs (tcgen05 kernel).
+// Decode step: the newest token row of each sequence, written by the plan
+// launch's CTAs 1.. while CTA 0 computes the prefix sums (key == nullptr: none).
+struct NewTokens {
+  const uint4 *key;
+  const uint4 *value;
+  uint4 *k_cache;
+  uint4 *v_cache;
+  const int32_t *block_tables;
+  int max_blocks_per_seq;
+  int block_size;
+  int num_blocks;
+  int row_vecs;              // 16-byte vectors per token row (Hkv * 128 bf16)
+  int64_t key_stride_vecs;
+  int64_t value_stride_vecs;
+};
+
 __global__ void __launch_bounds__(1024)
 decode_plan_kernel(const int32_t *__restrict__ context_lens, int num_seqs, int max_context_len,
-                   int grid, int units_per_token, int min_range, uint8_t *ws, uint32_t *err) {
+                   int grid, int units_per_token, int min_range, uint8_t *ws, uint32_t *err,
+                   NewTokens nt) {
   __shared__ int warp_sums[32];
   __shared__ int base;
   int *cu = reinterpret_cast<int *>(ws + 256);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (blockIdx.x > 0) {
+    // Decode step: one warp per sequence writes its newest token at logical
+    // position n - 1, n = context_lens[i] clamped to [0, max_context_len] as
+    // below (n = 0 writes nothing): row (n-1) % bs of block
+    // block_tables[i][(n-1) / bs]. The decode kernel that reads the cache is
+    // the next launch on the stream.
+    const int i = (blockIdx.x - 1) * 32 + warp;
+    if (i >= num_seqs) return;
+    int n = context_lens[i];
+    n = n < 0 ? 0 : (n > max_context_len ? max_context_len : n);
+    if (n == 0) return;
+    const int pos = n - 1;
+    const int blk = nt.block_tables[static_cast<int64_t>(i) * nt.max_blocks_per_seq + pos / nt.block_size];
+    if (blk < 0 || blk >= nt.num_blocks) {
+      if (lane == 0) raise_error(err, PKV_DEVERR_BLOCK_ID);
+      return;
+    }
+    const int64_t row = static_cast<int64_t>(blk) * nt.block_size + pos % nt.block_size;
+    for (int v = lane; v < nt.row_vecs; v += 32) {
+      nt.k_cache[row * nt.row_vecs + v] = __ldg(nt.key + i * nt.key_stride_vecs + v);
+      nt.v_cache[row * nt.row_vecs + v] = __ldg(nt.value + i * nt.value_stride_vecs + v);
+    }
+    return;
+  }
   if (threadIdx.x == 0) {
     base = 0;
     cu[0] = 0;
@@ -649,6 +690,31 @@ int split_grid(int num_q_heads, int num_kv_heads, cudaError_t *status) {
   return per_sm * sm_count(dev);
 }
 
+// The plan launch: CTA 0 plans the ranges; with new tokens (decode step), CTAs
+// 1.. write them, 32 sequences per CTA.
+cudaError_t launch_plan(const DecodeArgs &a, int grid, int units_per_token, int min_range,
+                        uint8_t *ws, cudaStream_t stream) {
+  NewTokens nt{};
+  unsigned ctas = 1;
+  if (a.key_new != nullptr) {
+    nt.key = static_cast<const uint4 *>(a.key_new);
+    nt.value = static_cast<const uint4 *>(a.value_new);
+    nt.k_cache = static_cast<uint4 *>(const_cast<void *>(a.k_cache));
+    nt.v_cache = static_cast<uint4 *>(const_cast<void *>(a.v_cache));
+    nt.block_tables = a.block_tables;
+    nt.max_blocks_per_seq = a.max_blocks_per_seq;
+    nt.block_size = a.block_size;
+    nt.num_blocks = a.num_blocks;
+    nt.row_vecs = a.num_kv_heads * (kHeadDim / 8);
+    nt.key_stride_vecs = a.key_stride / 8;
+    nt.value_stride_vecs = a.value_stride / 8;
+    ctas += static_cast<unsigned>((a.num_seqs + 31) / 32);
+  }
+  decode_plan_kernel<<<ctas, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len,
+                                                grid, units_per_token, min_range, ws, a.err, nt);
+  return cudaGetLastError();
+}
+
 size_t tc_workspace(int num_seqs, int group, int grid) {
   const size_t rows = size_t(2) * grid * group;
   const size_t ml = align256(256 + sizeof(int) * (size_t(num_seqs) + 1));
@@ -722,17 +788,9 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
   cp.group = group;
   cp.tc = plan.tc ? 1 : 0;
 
-  // Decode step: the tcgen05 all-heads kernel stores the new tokens itself;
-  // the other kernels get them from a store launch first (same stream order).
-  if (a.key_new != nullptr && plan.kind != 3 &&
-      (e = launch_store_new_tokens(a, stream)) != cudaSuccess)
-    return e;
-
   if (plan.kind == 3) {
     const WsLayout lay = ws_layout(a.num_seqs, a.num_q_heads, 1, grid);
-    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len, grid,
-                                               1, 128, ws, a.err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_plan(a, grid, 1, 128, ws, stream)) != cudaSuccess) return e;
     cp.wph = 1;
     cp.ml = reinterpret_cast<float2 *>(ws + lay.ml);
     cp.po = reinterpret_cast<float *>(ws + lay.o);
@@ -740,9 +798,7 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
                                reinterpret_cast<float *>(ws + lay.o), stream)) != cudaSuccess)
       return e;
   } else if (plan.kind == 2) {
-    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len, grid,
-                                               a.num_kv_heads, 128, ws, a.err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_plan(a, grid, a.num_kv_heads, 128, ws, stream)) != cudaSuccess) return e;
     const size_t ml = align256(256 + sizeof(int) * (size_t(a.num_seqs) + 1));
     const size_t o = align256(ml + sizeof(float2) * size_t(2) * grid * group);
     cp.ml = reinterpret_cast<float2 *>(ws + ml);
@@ -752,9 +808,7 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
       return e;
   } else {
     const WsLayout lay = ws_layout(a.num_seqs, a.num_q_heads, wph, grid);
-    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len, grid,
-                                               1, kMinRange, ws, a.err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_plan(a, grid, 1, kMinRange, ws, stream)) != cudaSuccess) return e;
     SplitParams sp;
     sp.out = static_cast<__nv_bfloat16 *>(a.out);
     sp.q = static_cast<const __nv_bfloat16 *>(a.q);

@@ -83,13 +83,6 @@ struct GParams {
   float2 *ml;
   float *po;
   uint32_t *err;
-  // decode step (key_new == nullptr otherwise): newest token rows and the cache
-  uint4 *k_rows;
-  uint4 *v_rows;
-  const uint4 *key_new;
-  const uint4 *value_new;
-  int64_t key_stride_vecs;
-  int64_t value_stride_vecs;
 };
 
 // shared-memory map, all offsets from a 1024-aligned base
@@ -256,37 +249,6 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), p.tmem_cols);
     tmem_relinquish();
-  }
-  if (p.key_new != nullptr && lo < hi) {
-    // Decode step: this CTA writes the newest token of every sequence whose last
-    // position (flat index cu[i+1] - 1) lies in its range, before its first TMA
-    // load. Only this CTA attends to that position; a neighbour's stage box may
-    // cover the row too, but masks it out of its own segment.
-    int a = 0, b = p.num_seqs;
-    while (a < b) {
-      const int m = (a + b) >> 1;
-      if (cu[m + 1] > lo) b = m;
-      else a = m + 1;
-    }
-    const int row_vecs = p.num_kv_heads * (kHD / 8);
-    for (int i = a; i < p.num_seqs && cu[i + 1] - 1 < hi; ++i) {
-      const int n = cu[i + 1] - cu[i];
-      if (n <= 0) continue;
-      const int pos = n - 1;
-      const int blk = p.block_tables[static_cast<int64_t>(i) * p.max_blocks_per_seq + pos / p.block_size];
-      if (blk < 0 || blk >= p.num_blocks) {
-        if (threadIdx.x == 0) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
-        continue;
-      }
-      const int64_t row = static_cast<int64_t>(blk) * p.block_size + pos % p.block_size;
-      for (int v = threadIdx.x; v < row_vecs; v += kThreads) {
-        p.k_rows[row * row_vecs + v] = __ldg(p.key_new + i * p.key_stride_vecs + v);
-        p.v_rows[row * row_vecs + v] = __ldg(p.value_new + i * p.value_stride_vecs + v);
-      }
-    }
-    // these generic-proxy writes must be visible to the TMA (async proxy) loads
-    // the producers issue after the barrier below
-    asm volatile("fence.proxy.async.global;" ::: "memory");
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -762,12 +724,6 @@ cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *
   p.ml = ml;
   p.po = po;
   p.err = a.err;
-  p.k_rows = static_cast<uint4 *>(const_cast<void *>(a.k_cache));
-  p.v_rows = static_cast<uint4 *>(const_cast<void *>(a.v_cache));
-  p.key_new = static_cast<const uint4 *>(a.key_new);
-  p.value_new = static_cast<const uint4 *>(a.value_new);
-  p.key_stride_vecs = a.key_stride / 8;
-  p.value_stride_vecs = a.value_stride / 8;
   auto kern = tcg_kernel_for(T, p.group);
   if (kern == nullptr) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -50,10 +50,6 @@ struct DecodeArgs {
   int64_t value_stride = 0;
 };
 
-// Writes each sequence's newest K/V row (DecodeArgs::key_new / value_new) at
-// its last logical position, one warp per sequence.
-cudaError_t launch_store_new_tokens(const DecodeArgs &a, cudaStream_t stream);
-
 // Which decode kernel runs and on how many CTAs. Block sizes that are a
 // multiple of 8 (and at most 16 query heads per KV head) run the tcgen05
 // kernel; other shapes the CUDA-core split kernel.

@@ -59,56 +59,7 @@ store_kvcache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ va
   }
 }
 
-// Decode step: sequence i's newest token goes to logical position n - 1 of
-// that sequence, n = context_lens[i] clamped to [0, max_context_len] (the same
-// clamp the decode plan applies; n = 0 stores nothing). Its slot is the one the
-// paging metadata names: block_tables[i][(n-1) / bs] * bs + (n-1) % bs. One warp
-// per sequence, 16-byte vectors.
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
-store_new_tokens_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
-                        uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
-                        const int32_t *__restrict__ block_tables, int32_t max_blocks_per_seq,
-                        const int32_t *__restrict__ context_lens, int32_t num_seqs,
-                        int32_t max_context_len, int32_t block_size, int32_t num_blocks,
-                        int32_t row_vecs, int64_t key_stride_vecs, int64_t value_stride_vecs,
-                        uint32_t *err) {
-  const int lane = threadIdx.x & 31;
-  const int i = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  if (i >= num_seqs) return;
-  int n = __ldg(context_lens + i);
-  n = n < 0 ? 0 : (n > max_context_len ? max_context_len : n);
-  if (n == 0) return;
-  const int pos = n - 1;
-  const int blk = __ldg(block_tables + static_cast<int64_t>(i) * max_blocks_per_seq + pos / block_size);
-  if (blk < 0 || blk >= num_blocks) {
-    if (lane == 0) raise_error(err, PKV_DEVERR_BLOCK_ID);
-    return;
-  }
-  const int64_t slot = static_cast<int64_t>(blk) * block_size + pos % block_size;
-  const uint4 *ks = key + i * key_stride_vecs;
-  const uint4 *vs = value + i * value_stride_vecs;
-  uint4 *kd = k_cache + slot * row_vecs;
-  uint4 *vd = v_cache + slot * row_vecs;
-  for (int v = lane; v < row_vecs; v += 32) {
-    kd[v] = __ldg(ks + v);
-    vd[v] = __ldg(vs + v);
-  }
-}
-
 }  // namespace
-
-cudaError_t launch_store_new_tokens(const DecodeArgs &a, cudaStream_t stream) {
-  if (a.num_seqs == 0) return cudaSuccess;
-  const int32_t row_vecs = a.num_kv_heads * 128 / 8;
-  const unsigned grid = static_cast<unsigned>((a.num_seqs + kWarpsPerCta - 1) / kWarpsPerCta);
-  store_new_tokens_kernel<<<grid, kWarpsPerCta * 32, 0, stream>>>(
-      static_cast<const uint4 *>(a.key_new), static_cast<const uint4 *>(a.value_new),
-      static_cast<uint4 *>(const_cast<void *>(a.k_cache)),
-      static_cast<uint4 *>(const_cast<void *>(a.v_cache)), a.block_tables, a.max_blocks_per_seq,
-      a.context_lens, a.num_seqs, a.max_context_len, a.block_size, a.num_blocks, row_vecs,
-      a.key_stride / 8, a.value_stride / 8, a.err);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_store_kvcache(const void *key, const void *value, void *k_cache, void *v_cache,
                                  const int32_t *slot_mapping, int32_t num_tokens,

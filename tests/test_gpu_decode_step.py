@@ -38,8 +38,8 @@ def run_step(w, t, m):
     return out
 
 
-# (Hkv, G, bs): the all-heads tcgen05 kernel (store fused into the decode
-# launch), the per-head tcgen05 kernel and the CUDA-core kernel (store launch first)
+# (Hkv, G, bs) covering the all-heads tcgen05 kernel, the per-head tcgen05
+# kernel and the CUDA-core kernel behind the step's planning launch
 SHAPES = [(8, 4, 16), (8, 4, 256), (4, 8, 32), (16, 2, 16), (8, 1, 16), (2, 4, 16),
           (3, 5, 32), (8, 4, 3), (4, 2, 1)]
 
