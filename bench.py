@@ -416,9 +416,46 @@ def run_pkv(args, rank, world, device):
     }
     result["prefill_row"] = measure_prefill(args, device, steps=max(5, min(args.steps, 20)))
     result["gpu_launches_prefill_row"] = 2 * max(5, min(args.steps, 20))
+    result["copy_blocks_row"] = measure_copy_blocks(device, steps=max(5, min(args.steps, 20)))
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_oracle_sample(w)
     return result
+
+
+def measure_copy_blocks(device, steps):
+    """The copy-on-write row: 4096 whole-block copies (random distinct source and
+    destination blocks of a 16-token, 8-KV-head pool), K and V: 512 MiB moved per
+    launch, more than L2, timed with CUDA events."""
+    import torch
+    import paged_kv_cache_86_gb300 as pkv
+    nb, bs, hkv, d, pairs = 16384, 16, 8, 128, 4096
+    g = torch.Generator(device=device).manual_seed(86009)
+    kc = torch.empty((nb, bs, hkv, d), dtype=torch.bfloat16, device=device).normal_(generator=g)
+    vc = torch.empty_like(kc).normal_(generator=g)
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(86010))
+    src = perm[:pairs].to(torch.int32).to(device)
+    dst = perm[pairs:2 * pairs].to(torch.int32).to(device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(3):
+        pkv.copy_blocks(kc, vc, src, dst)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pkv.copy_blocks(kc, vc, src, dst)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    if pkv.get_device_errors() != 0:
+        raise RuntimeError("device-side range check fired in the block-copy measurement")
+    ms = statistics.median(times)
+    nbytes = pairs * 2 * 2 * bs * hkv * d * 2      # K and V, read and write
+    hpeak, _ = measured_peaks()
+    return {"workload": f"copy_{pairs}_blocks_bs{bs}_hkv{hkv}", "bytes_per_launch": nbytes,
+            "ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hpeak,
+            "l2": "512 MiB per launch, larger than L2; median of launches"}
 
 
 def prefill_flops(w) -> int:

@@ -14,7 +14,8 @@
  *                      (pkv_decode_step: the store of each sequence's newest
  *                      token and the decode in one call);
  *   pkv_paged_prefill  varlen query chunks (cu_seqlens_q) over their cached
- *                      prefix plus themselves (cu_seqlens_k), causal.
+ *                      prefix plus themselves (cu_seqlens_k), causal;
+ *   pkv_copy_blocks    copy-on-write of shared cache blocks.
  *
  * Cache layout. One layer's K cache and V cache are two separate arrays of
  * shape [num_blocks, block_size, num_kv_heads, head_dim], row-major, bf16.
@@ -97,6 +98,29 @@ pkv_status pkv_store_kvcache(const void *key, const void *value,
                              int32_t block_size, int32_t num_blocks,
                              int64_t key_token_stride, int64_t value_token_stride,
                              pkv_dtype dtype, void *stream);
+
+/* ------------------------------------------------------------ block copy --
+ * pkv_copy_blocks: for p < num_pairs, rows 0 .. num_rows[p]-1 of physical block
+ * src_block_ids[p] are copied to the same rows of block dst_block_ids[p], in
+ * both k_cache and v_cache (whole blocks when num_rows is NULL). This is the
+ * copy-on-write step of prefix sharing: requests may point at the same
+ * read-only blocks, and before a request writes into a shared block that is
+ * not yet full it needs its own copy, or it would change another request's
+ * history (推理运行时 §Prefix cache 与 copy-on-write; nano vllm代码详解 §3
+ * Block / BlockManager keep shared blocks by reference count).
+ *   src_block_ids, dst_block_ids, num_rows   [num_pairs] int32, device.
+ *   num_pairs <= 65535. The dst blocks must be distinct and must not be
+ *   the src of any pair in the same call (the copies run concurrently).
+ * A block id outside [0, num_blocks) skips its pair and sets
+ * PKV_DEVERR_BLOCK_ID; a row count outside [0, block_size] is clamped and sets
+ * PKV_DEVERR_LENGTH.
+ */
+pkv_status pkv_copy_blocks(void *k_cache, void *v_cache,
+                           const int32_t *src_block_ids, const int32_t *dst_block_ids,
+                           const int32_t *num_rows, int32_t num_pairs,
+                           int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks,
+                           pkv_dtype dtype, void *stream);
 
 /* ---------------------------------------------------------------- decode --
  * out[i, g, :] = softmax_p(scale * q[i, g, :] . K_i[p, g / G, :]) . V_i[p, g / G, :]

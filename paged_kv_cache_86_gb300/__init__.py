@@ -6,8 +6,10 @@ binding plus the seeded synthetic workload generator used by tests and the
 bench. Importing the package does not load the library; the first call does,
 and fails loudly if it has not been built.
 """
-from ._lib import (PkvError, decode_step, decode_workspace_size, get_device_errors, load,
-                   paged_decode, paged_prefill, prefill_workspace_size, store_kvcache, version)
+from ._lib import (PkvError, copy_blocks, decode_step, decode_workspace_size, get_device_errors,
+                   load, paged_decode, paged_prefill, prefill_workspace_size, store_kvcache,
+                   version)
 
-__all__ = ["PkvError", "decode_step", "decode_workspace_size", "get_device_errors", "load",
-           "paged_decode", "paged_prefill", "prefill_workspace_size", "store_kvcache", "version"]
+__all__ = ["PkvError", "copy_blocks", "decode_step", "decode_workspace_size", "get_device_errors",
+           "load", "paged_decode", "paged_prefill", "prefill_workspace_size", "store_kvcache",
+           "version"]

@@ -59,6 +59,8 @@ def load(path: str = LIB_PATH):
                                          i32, i32, f32, vp, sz, ctypes.c_int, vp]
         lib.pkv_decode_step.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, i32, vp, i32, i32,
                                         i32, i32, i32, i32, i32, f32, vp, sz, ctypes.c_int, vp]
+        lib.pkv_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int,
+                                        vp]
         lib.pkv_prefill_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.pkv_prefill_workspace_size.restype = sz
         lib.pkv_paged_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, vp, i32, i32, i32,
@@ -69,7 +71,7 @@ def load(path: str = LIB_PATH):
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_version.restype = i32
         for name in ("pkv_store_kvcache", "pkv_paged_decode", "pkv_decode_step",
-                     "pkv_paged_prefill", "pkv_get_device_errors"):
+                     "pkv_paged_prefill", "pkv_copy_blocks", "pkv_get_device_errors"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -123,6 +125,36 @@ def store_kvcache(key, value, k_cache, v_cache, slot_mapping, stream=None) -> No
                                  _ptr(slot_mapping.contiguous()), t, hkv, d, bs, nb,
                                  key.stride(0), value.stride(0), PKV_BF16,
                                  _stream(k_cache, stream)), "pkv_store_kvcache")
+
+
+def copy_blocks(k_cache, v_cache, src_block_ids, dst_block_ids, num_rows=None,
+                stream=None) -> None:
+    """Copy rows [0, num_rows[p]) (whole blocks when num_rows is None) of block
+    src_block_ids[p] to block dst_block_ids[p] in both caches [NB, bs, Hkv, D]."""
+    lib = load()
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16, 4)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache / v_cache shape mismatch")
+    _need(src_block_ids, "src_block_ids", torch.int32, 1)
+    _need(dst_block_ids, "dst_block_ids", torch.int32, 1)
+    n = src_block_ids.shape[0]
+    if dst_block_ids.shape[0] != n:
+        raise ValueError("src / dst length mismatch")
+    rows_ptr = ctypes.c_void_p(0)
+    if num_rows is not None:
+        _need(num_rows, "num_rows", torch.int32, 1)
+        if num_rows.shape[0] != n:
+            raise ValueError("num_rows length mismatch")
+        num_rows = num_rows.contiguous()
+        rows_ptr = _ptr(num_rows)
+    nb, bs, hkv, d = k_cache.shape
+    src_block_ids, dst_block_ids = src_block_ids.contiguous(), dst_block_ids.contiguous()
+    _check(lib.pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src_block_ids),
+                               _ptr(dst_block_ids), rows_ptr, n, hkv, d, bs, nb, PKV_BF16,
+                               _stream(k_cache, stream)), "pkv_copy_blocks")
 
 
 def decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,

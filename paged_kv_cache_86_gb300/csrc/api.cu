@@ -87,6 +87,28 @@ pkv_status pkv_store_kvcache(const void *key, const void *value, void *k_cache, 
   return from_cuda(e);
 }
 
+pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_block_ids,
+                           const int32_t *dst_block_ids, const int32_t *num_rows,
+                           int32_t num_pairs, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, pkv_dtype dtype, void *stream) {
+  if (dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (num_pairs < 0 || num_pairs > 65535 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 ||
+      num_blocks < 1)
+    return PKV_ERR_ARG;
+  const int64_t row = int64_t(num_kv_heads) * head_dim;
+  if (row % 8 != 0) return PKV_ERR_SHAPE;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !src_block_ids || !dst_block_ids) return PKV_ERR_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ARG;
+  cudaError_t e;
+  uint32_t *err = pkv::device_error_word(&e);
+  if (!err) return PKV_ERR_CUDA;
+  return from_cuda(pkv::launch_copy_blocks(k_cache, v_cache, src_block_ids, dst_block_ids,
+                                           num_rows, num_pairs, block_size, num_blocks,
+                                           static_cast<int32_t>(row), err,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim) {
   if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim != 128 ||

@@ -21,6 +21,12 @@ cudaError_t launch_store_kvcache(const void *key, const void *value, void *k_cac
                                  int32_t row_elems, int64_t key_stride, int64_t value_stride,
                                  int64_t num_slots, uint32_t *err, cudaStream_t stream);
 
+// ---- block copy (copy-on-write)
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *src,
+                               const int32_t *dst, const int32_t *rows, int32_t num_pairs,
+                               int32_t block_size, int32_t num_blocks, int32_t row_elems,
+                               uint32_t *err, cudaStream_t stream);
+
 // ---- decode
 struct DecodeArgs {
   void *out;

@@ -88,3 +88,15 @@ def test_decode_step_host_validation_needs_no_gpu(lib):
     assert step(a, a, 128, 256) == -1                   # stride shorter than a row (2 x 128)
     assert step(a, a, 256, 256, scale=float("inf")) == -1
     assert step(null, null, 0, 0, num_seqs=0) == 0      # nothing to do
+
+
+def test_copy_blocks_host_validation_needs_no_gpu(lib):
+    vp, null = ctypes.c_void_p, ctypes.c_void_p(0)
+    a = vp(256)
+    assert lib.pkv_copy_blocks(a, a, a, a, null, 3, 8, 128, 16, 64, 7, null) == -3   # dtype
+    assert lib.pkv_copy_blocks(a, a, a, a, null, -1, 8, 128, 16, 64, 0, null) == -1  # count
+    assert lib.pkv_copy_blocks(a, a, a, a, null, 65536, 8, 128, 16, 64, 0, null) == -1
+    assert lib.pkv_copy_blocks(a, a, a, a, null, 3, 1, 12, 16, 64, 0, null) == -2    # row of 12
+    assert lib.pkv_copy_blocks(a, a, null, a, null, 3, 8, 128, 16, 64, 0, null) == -1  # no src
+    assert lib.pkv_copy_blocks(vp(264), a, a, a, null, 3, 8, 128, 16, 64, 0, null) == -1  # align
+    assert lib.pkv_copy_blocks(null, null, null, null, null, 0, 8, 128, 16, 64, 0, null) == 0
