@@ -50,7 +50,18 @@ def load_library(path: str):
                                       i64, i64, dbl, vp]
     lib.pkvo_paged_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64,
                                        i64, i64, i64, dbl, i32, vp]
-    for f in (lib.pkvo_store_kvcache, lib.pkvo_paged_decode, lib.pkvo_paged_prefill):
+    u8, f32 = ctypes.c_uint8, ctypes.c_float
+    lib.pkvo_e4m3_value.argtypes = [u8]
+    lib.pkvo_e4m3_value.restype = dbl
+    lib.pkvo_e4m3_encode.argtypes = [f32]
+    lib.pkvo_e4m3_encode.restype = u8
+    lib.pkvo_quantize_row_fp8.argtypes = [vp, i64, vp, vp]
+    lib.pkvo_quantize_row_fp8.restype = None
+    lib.pkvo_store_kvcache_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64]
+    lib.pkvo_paged_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, vp, i64, i64, i64,
+                                          i64, i64, i64, dbl, vp]
+    for f in (lib.pkvo_store_kvcache, lib.pkvo_paged_decode, lib.pkvo_paged_prefill,
+              lib.pkvo_store_kvcache_fp8, lib.pkvo_paged_decode_fp8):
         f.restype = ctypes.c_int
     lib.pkvo_max_threads.restype = ctypes.c_int
     lib.pkvo_set_threads.argtypes = [ctypes.c_int]
@@ -154,4 +165,73 @@ def paged_prefill(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables,
                                       _ptr(cu_q), _ptr(cu_k), _ptr(block_tables),
                                       block_tables.shape[1], s, hq, hkv, d, bs, nb, float(scale),
                                       1 if causal else 0, _ptr(mask)))
+    return out
+
+
+# ------------------------------------------------------------------ fp8 KV --
+
+def e4m3_value(code: int, lib=None) -> float:
+    """Value of one OCP FP8 E4M3 code (NaN for S.1111.111)."""
+    return float((lib or _load()).pkvo_e4m3_value(int(code) & 0xFF))
+
+
+def e4m3_encode(x: float, lib=None) -> int:
+    """Nearest finite E4M3 code of a float32 value, ties to even, saturating at 448."""
+    return int((lib or _load()).pkvo_e4m3_encode(float(np.float32(x))))
+
+
+def quantize_rows_fp8(x, lib=None):
+    """Rows of bf16 bits [R, D] -> (codes [R, D] uint8, scales [R] float32)."""
+    x = _c(x, np.uint16)
+    r, d = x.shape
+    codes = np.zeros((r, d), dtype=np.uint8)
+    scales = np.zeros(r, dtype=np.float32)
+    lib = lib or _load()
+    for i in range(r):
+        lib.pkvo_quantize_row_fp8(_ptr(x[i]), d, _ptr(codes[i]), _ptr(scales[i:i + 1]))
+    return codes, scales
+
+
+def store_kvcache_fp8(key, value, k_codes, v_codes, k_scales, v_scales, slot_mapping,
+                      block_size: int, lib=None) -> None:
+    """Quantize ``key``/``value`` [T, Hkv, D] (bf16 bits) into the fp8 caches
+    [NB, bs, Hkv, D] uint8 and their scales [NB * bs, Hkv] float32, in place."""
+    key, value = _c(key, np.uint16), _c(value, np.uint16)
+    slot_mapping = _c(slot_mapping, np.int32)
+    for a, dt in ((k_codes, np.uint8), (v_codes, np.uint8), (k_scales, np.float32),
+                  (v_scales, np.float32)):
+        if a.dtype != dt or not a.flags.c_contiguous:
+            raise TypeError("fp8 caches must be C-contiguous uint8, scales float32")
+    nb, bs, hkv, d = k_codes.shape
+    if bs != block_size or k_scales.shape != (nb * bs, hkv) or v_scales.shape != k_scales.shape:
+        raise ValueError("cache / scale shapes do not match")
+    t = slot_mapping.shape[0]
+    if key.shape != (t, hkv, d) or value.shape != (t, hkv, d):
+        raise ValueError("key/value shape mismatch")
+    _check((lib or _load()).pkvo_store_kvcache_fp8(
+        _ptr(key), _ptr(value), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales),
+        _ptr(slot_mapping), t, hkv, d, bs, nb))
+
+
+def paged_decode_fp8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens,
+                     scale: float, seq_mask=None, lib=None) -> np.ndarray:
+    """Decode attention over the dequantized fp8 cache: ``q`` [S, Hq, D] bf16 bits ->
+    out [S, Hq, D] float64 (NaN rows where seq_mask excludes a sequence)."""
+    q = _c(q, np.uint16)
+    k_codes, v_codes = _c(k_codes, np.uint8), _c(v_codes, np.uint8)
+    k_scales, v_scales = _c(k_scales, np.float32), _c(v_scales, np.float32)
+    block_tables = _c(block_tables, np.int32)
+    context_lens = _c(context_lens, np.int32)
+    s, hq, d = q.shape
+    nb, bs, hkv, d2 = k_codes.shape
+    if d2 != d or v_codes.shape != k_codes.shape or k_scales.shape != (nb * bs, hkv):
+        raise ValueError("cache shape mismatch")
+    if block_tables.ndim != 2 or block_tables.shape[0] != s or context_lens.shape != (s,):
+        raise ValueError("metadata shape mismatch")
+    mask = None if seq_mask is None else _c(np.asarray(seq_mask, dtype=np.uint8), np.uint8)
+    out = np.full((s, hq, d), np.nan, dtype=np.float64)
+    _check((lib or _load()).pkvo_paged_decode_fp8(
+        _ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales),
+        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), s, hq, hkv, d, bs, nb,
+        float(scale), _ptr(mask)))
     return out

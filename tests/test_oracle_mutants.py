@@ -28,6 +28,14 @@ MUTANTS = [
      "v_cache[dst + e] = key[t * row + e];"),
     ("context_excludes_new_token", "const int64_t n = context_lens[i];",
      "const int64_t n = context_lens[i] > 0 ? context_lens[i] - 1 : 0;"),
+    ("fp8_v_uses_k_scale", "const double vs = v_scales[slot * num_kv_heads + h];",
+     "const double vs = k_scales[slot * num_kv_heads + h];"),
+    ("fp8_ties_to_odd", "(err == best_err && (c & 1) == 0)", "(err == best_err && (c & 1) == 1)"),
+    ("fp8_exponent_bias", "ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    ("fp8_subnormal_step", "ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    ("fp8_scale_inverted", "volatile float sc = amax / 448.0f;", "volatile float sc = 448.0f / amax;"),
+    ("fp8_amax_not_abs", "const float a = fabsf(bf16_bits_to_float(x[d]));",
+     "const float a = bf16_bits_to_float(x[d]);"),
 ]
 
 
@@ -137,7 +145,56 @@ def _pin_sdpa_decode(lib):
     return ok
 
 
-PINS = [_pin_sdpa_decode, _pin_store, _pin_ctx_one, _pin_equal_keys, _pin_two_keys, _pin_prefill_equal_keys]
+def _pin_fp8_codes_match_torch(lib):
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    got = np.array([oracle.e4m3_value(c, lib=lib) for c in codes])
+    nan = np.isnan(ref)
+    if not (np.array_equal(nan, np.isnan(got)) and np.array_equal(got[~nan], ref[~nan])):
+        return False
+    x = np.concatenate([np.random.default_rng(11).uniform(-448, 448, 500),
+                        (ref[1:0x7E] + ref[2:0x7F]) / 2]).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    return np.array_equal(np.array([oracle.e4m3_encode(v, lib=lib) for v in x], np.uint8), want)
+
+
+def _pin_fp8_row_quantization(lib):
+    import torch
+    rng = np.random.default_rng(12)
+    x = to_bf16_bits(rng.normal(0, 3.0, (16, 64)))
+    codes, scales = oracle.quantize_rows_fp8(x, lib=lib)
+    xf = bits_to_f64(x)
+    amax = np.abs(xf).max(axis=1)
+    if not np.array_equal(scales, (amax.astype(np.float32) / np.float32(448.0)).astype(np.float32)):
+        return False
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    deq = vals * scales[:, None].astype(np.float64)
+    bound = np.maximum(2.0 ** -4 * np.abs(xf), 2.0 ** -10 * scales[:, None]) * (1 + 1e-6)
+    return bool((np.abs(deq - xf) <= bound).all())
+
+
+def _pin_fp8_exact_decode(lib):
+    from test_oracle_fp8 import representable_cache
+    rng = np.random.default_rng(13)
+    nb, bs, hkv, hq, d = 12, 4, 2, 4, 32
+    kc, vc = representable_cache(rng, nb, bs, hkv, d), representable_cache(rng, nb, bs, hkv, d)
+    k8 = np.zeros((nb, bs, hkv, d), np.uint8)
+    v8 = np.zeros_like(k8)
+    ks = np.zeros((nb * bs, hkv), np.float32)
+    vs = np.zeros_like(ks)
+    oracle.store_kvcache_fp8(kc.reshape(-1, hkv, d), vc.reshape(-1, hkv, d), k8, v8, ks, vs,
+                             np.arange(nb * bs, dtype=np.int32), bs, lib=lib)
+    tables = rng.permutation(nb).astype(np.int32).reshape(3, 4)
+    lens = np.array([3, 16, 9], np.int32)
+    q = to_bf16_bits(rng.standard_normal((3, hq, d)))
+    ref = oracle.paged_decode(q, kc, vc, tables, lens, 0.3, lib=lib)
+    got = oracle.paged_decode_fp8(q, k8, v8, ks, vs, tables, lens, 0.3, lib=lib)
+    return np.array_equal(got, ref)
+
+
+PINS = [_pin_sdpa_decode, _pin_store, _pin_ctx_one, _pin_equal_keys, _pin_two_keys, _pin_prefill_equal_keys,
+        _pin_fp8_codes_match_torch, _pin_fp8_row_quantization, _pin_fp8_exact_decode]
 
 
 def _run_pins(lib):
