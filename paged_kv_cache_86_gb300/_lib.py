@@ -59,6 +59,10 @@ def load(path: str = LIB_PATH):
                                          i32, i32, f32, vp, sz, ctypes.c_int, vp]
         lib.pkv_decode_step.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, i32, vp, i32, i32,
                                         i32, i32, i32, i32, i32, f32, vp, sz, ctypes.c_int, vp]
+        lib.pkv_store_kvcache_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                              i64, i64, vp]
+        lib.pkv_paged_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                             i32, i32, i32, i32, f32, vp, sz, vp]
         lib.pkv_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int,
                                         vp]
         lib.pkv_prefill_workspace_size.argtypes = [i32, i32, i32, i32]
@@ -71,7 +75,8 @@ def load(path: str = LIB_PATH):
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_version.restype = i32
         for name in ("pkv_store_kvcache", "pkv_paged_decode", "pkv_decode_step",
-                     "pkv_paged_prefill", "pkv_copy_blocks", "pkv_get_device_errors"):
+                     "pkv_paged_prefill", "pkv_copy_blocks", "pkv_store_kvcache_fp8",
+                     "pkv_paged_decode_fp8", "pkv_get_device_errors"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -125,6 +130,75 @@ def store_kvcache(key, value, k_cache, v_cache, slot_mapping, stream=None) -> No
                                  _ptr(slot_mapping.contiguous()), t, hkv, d, bs, nb,
                                  key.stride(0), value.stride(0), PKV_BF16,
                                  _stream(k_cache, stream)), "pkv_store_kvcache")
+
+
+def _need_fp8_cache(k_cache, v_cache, k_scales, v_scales):
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.uint8, 4)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache / v_cache shape mismatch")
+    nb, bs, hkv, d = k_cache.shape
+    for t, n in ((k_scales, "k_scales"), (v_scales, "v_scales")):
+        _need(t, n, torch.float32, 2)
+        if t.shape != (nb * bs, hkv) or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous [num_blocks * block_size, Hkv] tensor")
+    return nb, bs, hkv, d
+
+
+def store_kvcache_fp8(key, value, k_cache, v_cache, k_scales, v_scales, slot_mapping,
+                      stream=None) -> None:
+    """Quantize key/value [T, Hkv, 128] bf16 into the fp8 E4M3 caches [NB, bs, Hkv, 128]
+    (uint8 codes) and their row scales [NB * bs, Hkv] float32 at slot_mapping [T]."""
+    lib = load()
+    for t, n in ((key, "key"), (value, "value")):
+        _need(t, n, torch.bfloat16, 3)
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{n} rows must be contiguous [Hkv, D] blocks")
+    nb, bs, hkv, d = _need_fp8_cache(k_cache, v_cache, k_scales, v_scales)
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    t = slot_mapping.shape[0]
+    if key.shape != (t, hkv, d) or value.shape != (t, hkv, d):
+        raise ValueError("shape mismatch between key/value/caches/slot_mapping")
+    _check(lib.pkv_store_kvcache_fp8(_ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(k_scales), _ptr(v_scales),
+                                     _ptr(slot_mapping.contiguous()), t, hkv, d, bs, nb,
+                                     key.stride(0), value.stride(0), _stream(k_cache, stream)),
+           "pkv_store_kvcache_fp8")
+
+
+def paged_decode_fp8(q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens,
+                     scale: float, max_context_len: int | None = None, out=None, workspace=None,
+                     stream=None) -> torch.Tensor:
+    """Decode attention over fp8 E4M3 caches with row scales; returns out [S, Hq, 128] bf16."""
+    lib = load()
+    _need(q, "q", torch.bfloat16, 3)
+    nb, bs, hkv, d = _need_fp8_cache(k_cache, v_cache, k_scales, v_scales)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    if not (q.is_contiguous() and block_tables.is_contiguous() and context_lens.is_contiguous()):
+        raise ValueError("decode tensors must be contiguous")
+    s, hq, dq = q.shape
+    if dq != d:
+        raise ValueError("q / cache head_dim mismatch")
+    if block_tables.shape[0] != s or context_lens.shape[0] != s:
+        raise ValueError("metadata rows must equal the number of sequences")
+    mb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = mb * bs
+    if out is None:
+        out = torch.empty_like(q)
+    need = decode_workspace_size(s, hq, hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(lib.pkv_paged_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(k_scales), _ptr(v_scales), _ptr(block_tables), mb,
+                                    _ptr(context_lens), s, int(max_context_len), hq, hkv, d, bs, nb,
+                                    float(scale), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream(q, stream)), "pkv_paged_decode_fp8")
+    return out
 
 
 def copy_blocks(k_cache, v_cache, src_block_ids, dst_block_ids, num_rows=None,

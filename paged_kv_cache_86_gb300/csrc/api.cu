@@ -109,6 +109,33 @@ pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_bloc
                                            static_cast<cudaStream_t>(stream)));
 }
 
+pkv_status pkv_store_kvcache_fp8(const void *key, const void *value, void *k_cache, void *v_cache,
+                                 float *k_scales, float *v_scales, const int32_t *slot_mapping,
+                                 int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int32_t num_blocks, int64_t key_token_stride,
+                                 int64_t value_token_stride, void *stream) {
+  if (num_tokens < 0 || num_kv_heads < 1 || block_size < 1 || num_blocks < 1) return PKV_ERR_ARG;
+  if (head_dim != 128) return PKV_ERR_SHAPE;
+  const int64_t row = int64_t(num_kv_heads) * head_dim;
+  if (num_tokens == 0) return PKV_OK;
+  if (!key || !value || !k_cache || !v_cache || !k_scales || !v_scales || !slot_mapping)
+    return PKV_ERR_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(k_scales) || !aligned16(v_scales))
+    return PKV_ERR_ARG;
+  if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 != 0 ||
+      value_token_stride % 8 != 0)
+    return PKV_ERR_ARG;
+  cudaError_t e;
+  uint32_t *err = pkv::device_error_word(&e);
+  if (!err) return PKV_ERR_CUDA;
+  return from_cuda(pkv::launch_store_kvcache_fp8(key, value, k_cache, v_cache, k_scales, v_scales,
+                                                 slot_mapping, num_tokens, num_kv_heads,
+                                                 key_token_stride, value_token_stride,
+                                                 int64_t(num_blocks) * block_size, err,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
 size_t pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim) {
   if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim != 128 ||
@@ -129,8 +156,13 @@ pkv_status decode_call(void *out, const void *q, const void *key_new, const void
                        int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
                        int32_t max_context_len, int32_t num_q_heads, int32_t num_kv_heads,
                        int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
-                       void *workspace, size_t workspace_bytes, pkv_dtype dtype, void *stream) {
+                       void *workspace, size_t workspace_bytes, pkv_dtype dtype, void *stream,
+                       const float *k_scales = nullptr, const float *v_scales = nullptr) {
   if (dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  const bool fp8 = k_scales != nullptr || v_scales != nullptr;
+  if (fp8 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales) ||
+              key_new != nullptr))
+    return PKV_ERR_ARG;
   if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || block_size < 1 || num_blocks < 1 ||
       max_blocks_per_seq < 0 || max_context_len < 0 || !std::isfinite(scale))
     return PKV_ERR_ARG;
@@ -152,7 +184,7 @@ pkv_status decode_call(void *out, const void *q, const void *key_new, const void
   cudaError_t e;
   pkv::DecodePlan plan;
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_SHAPE;
-  if (!pkv::choose_decode_plan(num_q_heads, num_kv_heads, block_size, &plan, &e))
+  if (!pkv::choose_decode_plan(num_q_heads, num_kv_heads, block_size, &plan, &e, fp8))
     return e != cudaSuccess ? PKV_ERR_CUDA : PKV_ERR_SHAPE;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < pkv::decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, plan))
@@ -181,6 +213,9 @@ pkv_status decode_call(void *out, const void *q, const void *key_new, const void
   a.value_new = value_new;
   a.key_stride = key_stride;
   a.value_stride = value_stride;
+  a.fp8 = fp8;
+  a.k_scales = k_scales;
+  a.v_scales = v_scales;
   return from_cuda(pkv::launch_paged_decode(a, plan, static_cast<cudaStream_t>(stream)));
 }
 
@@ -199,6 +234,21 @@ pkv_status pkv_paged_decode(void *out, const void *q, const void *k_cache, const
                      max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_q_heads,
                      num_kv_heads, head_dim, block_size, num_blocks, scale, workspace,
                      workspace_bytes, dtype, stream);
+}
+
+pkv_status pkv_paged_decode_fp8(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                const float *k_scales, const float *v_scales,
+                                const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                const int32_t *context_lens, int32_t num_seqs,
+                                int32_t max_context_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                float scale, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+  if (num_seqs > 0 && (!k_scales || !v_scales)) return PKV_ERR_ARG;
+  return decode_call(out, q, nullptr, nullptr, 0, 0, k_cache, v_cache, block_tables,
+                     max_blocks_per_seq, context_lens, num_seqs, max_context_len, num_q_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, scale, workspace,
+                     workspace_bytes, PKV_BF16, stream, k_scales, v_scales);
 }
 
 pkv_status pkv_decode_step(void *out, const void *q, const void *key_new, const void *value_new,

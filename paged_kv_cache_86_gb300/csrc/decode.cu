@@ -723,8 +723,15 @@ size_t tc_workspace(int num_seqs, int group, int grid) {
 }
 
 bool choose_decode_plan(int num_q_heads, int num_kv_heads, int block_size, DecodePlan *plan,
-                        cudaError_t *status) {
+                        cudaError_t *status, bool fp8) {
   *status = cudaSuccess;
+  if (fp8) {  // quantized caches: the all-heads tcgen05 kernel only
+    if (!decode_tcg_supported(num_q_heads, num_kv_heads, block_size, true)) return false;
+    plan->kind = 3;
+    plan->tc = false;
+    plan->grid = decode_tc_grid();
+    return plan->grid > 0;
+  }
   if (decode_tcg_supported(num_q_heads, num_kv_heads, block_size)) {
     plan->kind = 3;
     plan->tc = false;

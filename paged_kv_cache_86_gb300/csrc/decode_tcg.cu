@@ -53,6 +53,10 @@ constexpr int kHD = 128;
 constexpr int kRegion = 16384;        // 128 rows x 128 B (one 64-dim half)
 constexpr int kKVBytes = 2 * kRegion;
 constexpr int kThreads = 224;  // K producer, MMA, 4 softmax warps, V producer
+// fp8 caches add two converter warpgroups (warps 7-10: K, 11-14: V)
+constexpr int kThreadsF8 = 480;
+constexpr int kRawCodes = 16384;      // one fp8 stage: 128 rows x 128 one-byte codes
+constexpr int kRawStage = 17408;      // codes + 128 fp32 row scales, padded to 1024 B
 constexpr int kMaxN = 128;
 constexpr int kMaxG = 16;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -83,14 +87,16 @@ struct GParams {
   float2 *ml;
   float *po;
   uint32_t *err;
+  const float *k_scales;  // fp8 caches: [NB * bs, Hkv] row scales
+  const float *v_scales;
 };
 
 // shared-memory map, all offsets from a 1024-aligned base
 struct GLayout {
-  int k, v, q, p, alpha, lsum, msum, desc, bar, total;
+  int k, v, q, p, alpha, lsum, msum, desc, bar, vflag, kr, vr, total;
 };
 
-__host__ __device__ inline GLayout g_layout(int stages, int n_cols) {
+__host__ __device__ inline GLayout g_layout(int stages, int n_cols, bool f8 = false) {
   GLayout L;
   const int small = n_cols * 128;         // one 64-dim half of Q^T / P^T (N rows x 128 B)
   L.k = 0;
@@ -102,7 +108,14 @@ __host__ __device__ inline GLayout g_layout(int stages, int n_cols) {
   L.msum = L.lsum + kMaxN * 4;            // [kMaxN] maxima
   L.desc = L.msum + kMaxN * 4;
   L.bar = L.desc + 4 * 32;
-  L.total = L.bar + 24 * 8 + 16;
+  L.vflag = L.bar + 32 * 8 + 16;          // 32 barriers, TMEM slot + abort flag, then V stage flags
+  L.total = L.vflag + 16;
+  L.kr = L.vr = 0;
+  if (f8) {                               // raw fp8 rings, 1024-aligned for the 128-byte swizzle
+    L.kr = (L.total + 1023) & ~1023;
+    L.vr = L.kr + stages * kRawStage;
+    L.total = L.vr + stages * kRawStage;
+  }
   return L;
 }
 
@@ -173,22 +186,75 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const v
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
+__device__ __forceinline__ void st_shared_f16(uint32_t addr, float v) {
+  const __half h = __float2half_rn(v);
+  asm volatile("st.shared.b16 [%0], %1;" :: "r"(addr), "h"(*reinterpret_cast<const unsigned short *>(&h))
+               : "memory");
+}
+
+// Two E4M3 codes (low byte first in memory) -> two f16 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(codes));
+  return h;
+}
+
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 c) {
+  uint4 r;
+  r.x = e4m3x2_to_f16x2(static_cast<uint16_t>(c.x & 0xffffu));
+  r.y = e4m3x2_to_f16x2(static_cast<uint16_t>(c.x >> 16));
+  r.z = e4m3x2_to_f16x2(static_cast<uint16_t>(c.y & 0xffffu));
+  r.w = e4m3x2_to_f16x2(static_cast<uint16_t>(c.y >> 16));
+  return r;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+               :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// Row r of a raw fp8 stage (128-byte rows, 128-byte swizzle: chunk c of row r
+// sits at chunk c ^ (r & 7)) -> row r of the f16 operand stage (two 64-dim
+// regions of 128-byte rows with the same swizzle), the layout the bf16 TMA
+// boxes produce.
+__device__ __forceinline__ void convert_row_e4m3(uint32_t raw, uint32_t cv, int r) {
+  const uint32_t sw = static_cast<uint32_t>(r & 7);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 w = lds128(raw + r * 128 + ((c ^ sw) << 4));       // dims 16c .. 16c+15
+    const uint32_t row = cv + (c >> 2) * kRegion + r * 128;
+    const uint32_t c2 = static_cast<uint32_t>((2 * c) & 7);
+    sts128(row + ((c2 ^ sw) << 4), e4m3x8_to_f16x8(make_uint2(w.x, w.y)));
+    sts128(row + (((c2 + 1) ^ sw) << 4), e4m3x8_to_f16x8(make_uint2(w.z, w.w)));
+  }
+}
+
+// bf16 -> f16 in place (exact for values of normal f16 magnitude)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const float2 f = bf16x2_to_float2(w);
+  uint32_t h;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(f.y), "f"(f.x));  // first operand -> upper half
+  return h;
+}
+
 __device__ __forceinline__ void st_shared_b16(uint32_t addr, float v) {
   const __nv_bfloat16 h = __float2bfloat16_rn(v);
   asm volatile("st.shared.b16 [%0], %1;" :: "r"(addr), "h"(*reinterpret_cast<const unsigned short *>(&h))
                : "memory");
 }
 
-// T: tokens per stage (128 / Hkv); G: query heads per KV head.
-template <int T, int G>
-__global__ void __launch_bounds__(kThreads, 1)
+// T: tokens per stage (128 / Hkv); G: query heads per KV head; F8: the caches
+// hold E4M3 codes with per-row scales (operands converted to f16 on chip).
+template <int T, int G, bool F8>
+__global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
 decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const GParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t *smem = smem_raw + (base - raw_addr);
-  const GLayout L = g_layout(p.stages, p.n_cols);
+  constexpr int NT = F8 ? kThreadsF8 : kThreads;
+  const GLayout L = g_layout(p.stages, p.n_cols, F8);
   const int N = p.n_cols;
   const int S = p.stages;
   const uint32_t small = N * 128;
@@ -215,7 +281,12 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t pv_done = bar0 + 8u * 13;
   const uint32_t x_bar = bar0 + 8u * 14;    // per-stage exchange among the softmax warps
   const uint32_t l_bar = bar0 + 8u * 15;    // per-segment row-sum exchange
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bar + 24 * 8);
+  // fp8: the loaders' copies land on kr_full / vr_full; the converters then
+  // fill the f16 stage and arrive on k_full / v_full
+  auto kr_full = [&](int s) { return bar0 + 8u * (24 + s); };
+  auto vr_full = [&](int s) { return bar0 + 8u * (28 + s); };
+  volatile int *vflag = reinterpret_cast<volatile int *>(smem + L.vflag);  // V stage flags
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bar + 32 * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   GDesc *desc = reinterpret_cast<GDesc *>(smem + L.desc);
   float *alpha_buf = reinterpret_cast<float *>(smem + L.alpha);          // [2][kMaxN]
@@ -225,15 +296,19 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t sK = base + L.k, sV = base + L.v, sQ = base + L.q, sP = base + L.p;
 
   // Q^T and P^T padding rows/columns must read as zeros for the whole kernel
-  for (int i = threadIdx.x; i < (6 * static_cast<int>(small)) / 16; i += kThreads)
+  for (int i = threadIdx.x; i < (6 * static_cast<int>(small)) / 16; i += NT)
     reinterpret_cast<uint4 *>(smem + L.q)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x < 2) grow_flag[threadIdx.x] = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(k_full(s), 1);
+      mbar_init(k_full(s), F8 ? 4 : 1);
       mbar_init(k_empty(s), 1 + 4);
-      mbar_init(v_full(s), 1);
+      mbar_init(v_full(s), F8 ? 4 : 1);
       mbar_init(v_empty(s), 1);
+      if (F8) {
+        mbar_init(kr_full(s), 1);
+        mbar_init(vr_full(s), 1);
+      }
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
@@ -284,7 +359,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       int good = 1;
       if (lane == 0) {
         const uint32_t empty = is_k ? k_empty(s) : v_empty(s);
-        const uint32_t full = is_k ? k_full(s) : v_full(s);
+        const uint32_t full = F8 ? (is_k ? kr_full(s) : vr_full(s)) : (is_k ? k_full(s) : v_full(s));
         // a Q^T buffer may only be refilled once the S MMAs of the previous
         // segment that used it are done (the slot wait covers stage issued - S)
         const int prev_q = (is_k && with_q) ? q_last[d.qbuf] : -1;
@@ -297,10 +372,12 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           fail();
         } else {
           const bool load = !(d.flags & kEnd) && blk_row >= 0;
-          uint32_t bytes = load ? 2 * kRegion : 0;
+          uint32_t bytes = load ? (F8 ? kRawCodes + kRows * 4 : 2 * kRegion) : 0;
           if (is_k) {
             desc[s] = d;
             if (with_q) bytes += 2 * p.num_q_heads * 128;
+          } else if (F8) {
+            vflag[s] = d.flags;
           }
           if (bytes) mbar_arrive_expect_tx(full, bytes);
           else mbar_arrive(full);
@@ -309,7 +386,14 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tma_load_3d(qdst, &tm_q, 0, 0, d.seq, full);
             tma_load_3d(qdst + small, &tm_q, 64, 0, d.seq, full);
           }
-          if (load) {
+          if (load && F8) {
+            // 128 rows of 128 codes in one box, then the rows' 128 scales
+            const uint32_t dst = base + (is_k ? L.kr : L.vr) + s * kRawStage;
+            tma_load_3d(dst, is_k ? &tm_k : &tm_v, 0, blk_row, 0, full);
+            const float *sc = (is_k ? p.k_scales : p.v_scales) +
+                              static_cast<int64_t>(blk_row) * p.num_kv_heads;
+            bulk_g2s(dst + kRawCodes, sc, kRows * 4, full, l2_policy_evict_first());
+          } else if (load) {
             const uint32_t dst = (is_k ? sK : sV) + s * kKVBytes;
             const CUtensorMap *map = is_k ? &tm_k : &tm_v;
             tma_load_3d(dst, map, 0, blk_row, 0, full);
@@ -374,14 +458,19 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ok = stage(e, -1, false);
     }
     if (lane == 0) {  // drain: the last copies must land before the CTA exits
-      for (int j = max(0, issued - S); j < issued; ++j)
-        mbar_wait(is_k ? k_full(j % S) : v_full(j % S), (j / S) & 1, nullptr);
+      for (int j = max(0, issued - S); j < issued; ++j) {
+        const int sj = j % S;
+        mbar_wait(F8 ? (is_k ? kr_full(sj) : vr_full(sj)) : (is_k ? k_full(sj) : v_full(sj)),
+                  (j / S) & 1, nullptr);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_s = umma_idesc_bf16(kRows, N, false);
-      const uint32_t idesc_pv = umma_idesc_bf16(kHD, N, false) | (1u << 15);  // A (V) MN-major
+      // fp8 caches: both operands of both MMAs are f16 (A/B format fields 0)
+      constexpr uint32_t kFmt = F8 ? ~((1u << 7) | (1u << 10)) : ~0u;
+      const uint32_t idesc_s = umma_idesc_bf16(kRows, N, false) & kFmt;
+      const uint32_t idesc_pv = (umma_idesc_bf16(kHD, N, false) | (1u << 15)) & kFmt;  // A (V) MN-major
       bool ok = true;
       int pv_issued = 0, s_issued = 0;
       int prev_s = 0, prev_first = 0;
@@ -424,6 +513,40 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (pv_issued > 0) mbar_wait(pv_done, (pv_issued - 1) & 1, nullptr);
     }
     __syncwarp();
+  } else if (F8 && warp >= 7) {
+    // ------------------------------------------------------------ converters
+    // Warps 7-10 expand each raw K stage, warps 11-14 each raw V stage, one
+    // 128-code row per thread, from E4M3 into the f16 operand layout (and, at
+    // a segment's first stage, the new Q^T buffer from bf16 to f16 in place).
+    const bool is_k = warp < 11;
+    const int r = static_cast<int>(threadIdx.x) - (is_k ? 224 : 352);
+    for (int j = 0;; ++j) {
+      const int s = j % S;
+      if (!warp_wait(is_k ? kr_full(s) : vr_full(s), (j / S) & 1, abort_flag)) {
+        fail();
+        break;
+      }
+      const int flags = is_k ? desc[s].flags : vflag[s];
+      if (flags & kEnd) {
+        __syncwarp();
+        if (is_k && lane == 0) mbar_arrive(k_full(s));  // lets the MMA and softmax see the end
+        break;
+      }
+      convert_row_e4m3(base + (is_k ? L.kr : L.vr) + s * kRawStage,
+                       (is_k ? sK : sV) + s * kKVBytes, r);
+      if (is_k && (flags & kFirst)) {
+        const uint32_t qbuf = sQ + desc[s].qbuf * 2 * small;
+        for (int i = r; i < static_cast<int>(small) / 8; i += 128) {  // 2 * small bytes, 16 per chunk
+          uint4 w = lds128(qbuf + i * 16);
+          w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
+                         bf16x2_to_f16x2(w.w));
+          sts128(qbuf + i * 16, w);
+        }
+      }
+      fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(is_k ? k_full(s) : v_full(s));
+    }
   } else {
     // --------------------------------------------------------------- softmax
     const int quad = warp & 3;                  // TMEM lane quadrant of this warp
@@ -450,6 +573,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const int s = j % S;
       if (!warp_wait(k_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
       const GDesc d = desc[s];
+      // fp8: this row's K scale sits in the raw stage, which the loader may
+      // refill once every softmax warp has arrived on k_empty
+      float kscale = 1.f;
+      if (F8 && !(d.flags & kEnd))
+        kscale = reinterpret_cast<const float *>(smem + L.kr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
       __syncwarp();
       if (lane == 0) mbar_arrive(k_empty(s));  // this stage's descriptor has been read
       if (d.flags & kEnd) break;
@@ -478,7 +606,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       float vmax[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        sc[g] = valid ? sc[g] * p.scale_log2 : -INFINITY;
+        sc[g] = valid ? sc[g] * (F8 ? p.scale_log2 * kscale : p.scale_log2) : -INFINITY;
         vmax[g] = sc[g];
       }
       // stage maximum of each query head over the T rows of its KV head (one warp)
@@ -511,15 +639,19 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (!warp_wait(pv_done, (j - 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
       }
+      const bool partial = d.pa < d.p0 || d.pa + T > d.p1;
+      // fp8: P^T rows carry the V row scale, read from the raw V stage
+      if ((F8 || partial) && !warp_wait(v_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
+      float vscale = 1.f;
+      if (F8) vscale = reinterpret_cast<const float *>(smem + L.vr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const int n = head * G + g;
-        st_shared_b16(p_region + (n >> 3) * 1024 + (n & 7) * 128 +
-                          ((((rc >> 3) ^ (n & 7)) << 4) | ((rc & 7) << 1)),
-                      pr[g]);
+        const uint32_t addr = p_region + (n >> 3) * 1024 + (n & 7) * 128 +
+                              ((((rc >> 3) ^ (n & 7)) << 4) | ((rc & 7) << 1));
+        if (F8) st_shared_f16(addr, pr[g] * vscale);
+        else st_shared_b16(addr, pr[g]);
       }
-      const bool partial = d.pa < d.p0 || d.pa + T > d.p1;
-      if (partial && !warp_wait(v_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
       if (!valid) {  // masked row: its V row must be zero for the PV MMA
         const uint32_t vrow = sV + s * kKVBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
@@ -632,61 +764,72 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool encode(CUtensorMap *map, const void *ptr, const cuuint64_t (&dims)[3],
-            const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3]) {
+            const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3],
+            CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+  return fn(map, type, 3, const_cast<void *>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 using TcgKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const GParams);
 
-template <int T>
+template <int T, bool F8>
 TcgKernel tcg_kernel_for_g(int g) {
   switch (g) {
-    case 1: return decode_tcg_kernel<T, 1>;
-    case 2: return decode_tcg_kernel<T, 2>;
-    case 4: return decode_tcg_kernel<T, 4>;
-    case 8: return decode_tcg_kernel<T, 8>;
+    case 1: return decode_tcg_kernel<T, 1, F8>;
+    case 2: return decode_tcg_kernel<T, 2, F8>;
+    case 4: return decode_tcg_kernel<T, 4, F8>;
+    case 8: return decode_tcg_kernel<T, 8, F8>;
     default: return nullptr;
   }
 }
 
-// instantiated shapes: T in {8, 16, 32} (Hkv 16, 8, 4), G in {1, 2, 4, 8}
-TcgKernel tcg_kernel_for(int t, int g) {
+// instantiated shapes: T in {8, 16, 32} (Hkv 16, 8, 4), G in {1, 2, 4, 8}; the
+// fp8 variant for T 16 (Hkv 8) and 32 (Hkv 4)
+TcgKernel tcg_kernel_for(int t, int g, bool f8) {
+  if (f8) {
+    switch (t) {
+      case 16: return tcg_kernel_for_g<16, true>(g);
+      case 32: return tcg_kernel_for_g<32, true>(g);
+      default: return nullptr;
+    }
+  }
   switch (t) {
-    case 8: return tcg_kernel_for_g<8>(g);
-    case 16: return tcg_kernel_for_g<16>(g);
-    case 32: return tcg_kernel_for_g<32>(g);
+    case 8: return tcg_kernel_for_g<8, false>(g);
+    case 16: return tcg_kernel_for_g<16, false>(g);
+    case 32: return tcg_kernel_for_g<32, false>(g);
     default: return nullptr;
   }
 }
 
-int pick_stages(int n_cols) {
-  for (int s = 3; s >= 2; --s)
-    if (g_layout(s, n_cols).total + 1024 <= 227 * 1024) return s;
+// fp8 keeps two stages: the raw rings take the room of the third
+int pick_stages(int n_cols, bool f8) {
+  for (int s = f8 ? 2 : 3; s >= 2; --s)
+    if (g_layout(s, n_cols, f8).total + 1024 <= 227 * 1024) return s;
   return 0;
 }
 
 }  // namespace
 
-bool decode_tcg_supported(int num_q_heads, int num_kv_heads, int block_size) {
+bool decode_tcg_supported(int num_q_heads, int num_kv_heads, int block_size, bool fp8) {
   if (num_kv_heads != 4 && num_kv_heads != 8 && num_kv_heads != 16) return false;
   if (num_q_heads % num_kv_heads != 0) return false;
-  if (tcg_kernel_for(kRows / num_kv_heads, num_q_heads / num_kv_heads) == nullptr) return false;
+  if (tcg_kernel_for(kRows / num_kv_heads, num_q_heads / num_kv_heads, fp8) == nullptr) return false;
   const int n_cols = (num_q_heads + 15) / 16 * 16;
   if (n_cols > kMaxN) return false;
   const int T = kRows / num_kv_heads;
-  return block_size % T == 0 && pick_stages(n_cols) > 0;
+  return block_size % T == 0 && pick_stages(n_cols, fp8) > 0;
 }
 
 cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *po,
                               cudaStream_t stream) {
   const int n_cols = (a.num_q_heads + 15) / 16 * 16;
-  const int stages = pick_stages(n_cols);
-  const size_t smem = g_layout(stages, n_cols).total + 1024;
+  const bool f8 = a.fp8;
+  const int stages = pick_stages(n_cols, f8);
+  const size_t smem = g_layout(stages, n_cols, f8).total + 1024;
   cudaError_t e = cudaSuccess;
   const int T = kRows / a.num_kv_heads;
   CUtensorMap tq, tk, tv;
@@ -700,9 +843,15 @@ cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *
   const cuuint64_t cd[3] = {kHD, cache_rows, hkv};
   const cuuint64_t cs[2] = {hkv * kHD * 2, kHD * 2};
   const cuuint32_t cb[3] = {64, static_cast<cuuint32_t>(T), static_cast<cuuint32_t>(hkv)};
-  if (!encode(&tq, a.q, qd, qs, qb) || !encode(&tk, a.k_cache, cd, cs, cb) ||
-      !encode(&tv, a.v_cache, cd, cs, cb))
-    return cudaErrorInvalidValue;
+  // fp8 cache: one-byte codes, a box of all 128 dims is one 128-byte swizzle row
+  const cuuint64_t cs8[2] = {hkv * kHD, kHD};
+  const cuuint32_t cb8[3] = {kHD, static_cast<cuuint32_t>(T), static_cast<cuuint32_t>(hkv)};
+  const bool maps_ok =
+      encode(&tq, a.q, qd, qs, qb) &&
+      (f8 ? encode(&tk, a.k_cache, cd, cs8, cb8, CU_TENSOR_MAP_DATA_TYPE_UINT8) &&
+                encode(&tv, a.v_cache, cd, cs8, cb8, CU_TENSOR_MAP_DATA_TYPE_UINT8)
+          : encode(&tk, a.k_cache, cd, cs, cb) && encode(&tv, a.v_cache, cd, cs, cb));
+  if (!maps_ok) return cudaErrorInvalidValue;
   int tmem_cols = 32;
   while (tmem_cols < 3 * n_cols + 16) tmem_cols <<= 1;
   GParams p;
@@ -724,11 +873,13 @@ cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *
   p.ml = ml;
   p.po = po;
   p.err = a.err;
-  auto kern = tcg_kernel_for(T, p.group);
+  p.k_scales = a.k_scales;
+  p.v_scales = a.v_scales;
+  auto kern = tcg_kernel_for(T, p.group, f8);
   if (kern == nullptr) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  kern<<<grid, f8 ? kThreadsF8 : kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

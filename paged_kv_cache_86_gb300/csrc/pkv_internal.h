@@ -21,6 +21,14 @@ cudaError_t launch_store_kvcache(const void *key, const void *value, void *k_cac
                                  int32_t row_elems, int64_t key_stride, int64_t value_stride,
                                  int64_t num_slots, uint32_t *err, cudaStream_t stream);
 
+// fp8 E4M3 caches [NB, bs, Hkv, 128] uint8 with fp32 scales [NB * bs, Hkv];
+// head_dim 128; strides in elements of the bf16 key/value rows.
+cudaError_t launch_store_kvcache_fp8(const void *key, const void *value, void *k_cache,
+                                     void *v_cache, float *k_scales, float *v_scales,
+                                     const int32_t *slot_mapping, int32_t num_tokens,
+                                     int32_t num_kv_heads, int64_t key_stride, int64_t value_stride,
+                                     int64_t num_slots, uint32_t *err, cudaStream_t stream);
+
 // ---- block copy (copy-on-write)
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *src,
                                const int32_t *dst, const int32_t *rows, int32_t num_pairs,
@@ -54,6 +62,10 @@ struct DecodeArgs {
   const void *value_new = nullptr;
   int64_t key_stride = 0;
   int64_t value_stride = 0;
+  // fp8 E4M3 caches (uint8 codes) with fp32 row scales [NB * bs, Hkv]
+  bool fp8 = false;
+  const float *k_scales = nullptr;
+  const float *v_scales = nullptr;
 };
 
 // Which decode kernel runs and on how many CTAs. Block sizes that are a
@@ -66,7 +78,7 @@ struct DecodePlan {
 };
 
 bool choose_decode_plan(int num_q_heads, int num_kv_heads, int block_size, DecodePlan *plan,
-                        cudaError_t *status);
+                        cudaError_t *status, bool fp8 = false);
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                               const DecodePlan &plan);
 // The largest workspace any block size needs for this head configuration.
@@ -75,7 +87,7 @@ size_t decode_workspace_upper_bound(int num_seqs, int num_q_heads, int num_kv_he
 cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
 
 // tcgen05 decode kernel, all KV heads of a block per stage (decode_tcg.cu)
-bool decode_tcg_supported(int num_q_heads, int num_kv_heads, int block_size);
+bool decode_tcg_supported(int num_q_heads, int num_kv_heads, int block_size, bool fp8 = false);
 cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *po,
                               cudaStream_t stream);
 

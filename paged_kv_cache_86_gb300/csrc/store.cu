@@ -59,7 +59,78 @@ store_kvcache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ va
   }
 }
 
+// fp8 E4M3 store: each (token, KV head) row of 128 values is quantized with
+// its own fp32 scale, amax / 448, and codes E4M3(x * (448 / amax)) rounded to
+// nearest even with saturation (cvt.rn.satfinite); a zero row gives zero codes
+// and scale 0 (LLM Infra 101 v0.2, KV Quantization: the cache stores low-bit
+// values instead of bf16). One warp per token; lane l holds dims 4l..4l+3.
+__device__ __forceinline__ uint32_t quantize4_e4m3(uint2 bits, float inv) {
+  const float2 lo = bf16x2_to_float2(bits.x), hi = bf16x2_to_float2(bits.y);
+  uint16_t c01, c23;
+  // cvt packs its first operand into the upper byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c01) : "f"(__fmul_rn(lo.y, inv)), "f"(__fmul_rn(lo.x, inv)));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c23) : "f"(__fmul_rn(hi.y, inv)), "f"(__fmul_rn(hi.x, inv)));
+  return static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
+}
+
+__device__ __forceinline__ void quantize_row_e4m3(const uint2 *src, uint32_t *codes, float *scale,
+                                                  int lane) {
+  const uint2 bits = __ldg(src + lane);
+  const float2 lo = bf16x2_to_float2(bits.x), hi = bf16x2_to_float2(bits.y);
+  float amax = fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(hi.x), fabsf(hi.y)));
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  uint32_t c = 0u;
+  float sc = 0.f;
+  if (amax > 0.f) {
+    const float inv = __fdiv_rn(448.f, amax);
+    sc = __fdiv_rn(amax, 448.f);
+    c = quantize4_e4m3(bits, inv);
+  }
+  codes[lane] = c;
+  if (lane == 0) *scale = sc;
+}
+
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+store_kvcache_fp8_kernel(const __nv_bfloat16 *__restrict__ key,
+                         const __nv_bfloat16 *__restrict__ value, uint8_t *__restrict__ k_cache,
+                         uint8_t *__restrict__ v_cache, float *__restrict__ k_scales,
+                         float *__restrict__ v_scales, const int32_t *__restrict__ slot_mapping,
+                         int32_t num_tokens, int32_t num_kv_heads, int64_t key_stride,
+                         int64_t value_stride, int64_t num_slots, uint32_t *err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  if (t >= num_tokens) return;
+  const int64_t slot = __ldg(slot_mapping + t);
+  if (slot < 0) return;  // padded token
+  if (slot >= num_slots) {
+    if (lane == 0) raise_error(err, PKV_DEVERR_SLOT);
+    return;
+  }
+  for (int h = 0; h < num_kv_heads; ++h) {
+    const int64_t row = slot * num_kv_heads + h;
+    quantize_row_e4m3(reinterpret_cast<const uint2 *>(key + t * key_stride + h * 128),
+                      reinterpret_cast<uint32_t *>(k_cache + row * 128), k_scales + row, lane);
+    quantize_row_e4m3(reinterpret_cast<const uint2 *>(value + t * value_stride + h * 128),
+                      reinterpret_cast<uint32_t *>(v_cache + row * 128), v_scales + row, lane);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_store_kvcache_fp8(const void *key, const void *value, void *k_cache,
+                                     void *v_cache, float *k_scales, float *v_scales,
+                                     const int32_t *slot_mapping, int32_t num_tokens,
+                                     int32_t num_kv_heads, int64_t key_stride, int64_t value_stride,
+                                     int64_t num_slots, uint32_t *err, cudaStream_t stream) {
+  if (num_tokens == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>((num_tokens + kWarpsPerCta - 1) / kWarpsPerCta);
+  store_kvcache_fp8_kernel<<<grid, kWarpsPerCta * 32, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(key), static_cast<const __nv_bfloat16 *>(value),
+      static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), k_scales, v_scales,
+      slot_mapping, num_tokens, num_kv_heads, key_stride, value_stride, num_slots, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_store_kvcache(const void *key, const void *value, void *k_cache, void *v_cache,
                                  const int32_t *slot_mapping, int32_t num_tokens,

@@ -112,6 +112,23 @@ def _normal_bf16(shape, seed: int, device) -> torch.Tensor:
     return x.to(torch.bfloat16)
 
 
+def fp8_pool(num_blocks: int, block_size: int, num_kv_heads: int, seed: int, head_dim: int = 128,
+             device=None):
+    """A random pre-filled fp8 cache for one of K or V: uint8 codes uniform over
+    the 254 finite E4M3 codes (every byte except 0x7F and 0xFF) and fp32 row
+    scales |N(0,1)| * 2 / 448 + 1e-3 per (slot, KV head). Plain seeded random
+    bytes and floats; nothing here quantizes anything."""
+    dev = device or "cuda"
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed))
+    codes = torch.randint(0, 254, (num_blocks, block_size, num_kv_heads, head_dim),
+                          generator=g, device=dev, dtype=torch.int32)
+    codes = torch.where(codes >= 0x7F, codes + 1, codes).to(torch.uint8)  # 0..126, 128..254
+    scales = torch.randn((num_blocks * block_size, num_kv_heads), generator=g, device=dev)
+    scales = scales.abs() * (2.0 / 448.0) + 1e-3
+    return codes, scales.float()
+
+
 def _align32(n: int) -> int:
     return (n + 31) // 32 * 32
 

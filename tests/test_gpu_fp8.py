@@ -1,0 +1,101 @@
+"""GPU parity of the fp8 (E4M3, per token-head scale) KV path against the
+oracle: the quantizing store bit for bit (codes and scales), and decode over
+the quantized cache within |gpu - oracle| <= 1e-2 * max(1, |oracle|)."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_86_gb300 as pkv
+from oracle import attention as oracle
+from paged_kv_cache_86_gb300 import workloads as W
+from paged_kv_cache_86_gb300.workloads import bf16_to_u16
+from pkv_testutil import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def fp8_case(w, seed):
+    kc, ks = W.fp8_pool(w.num_blocks, w.block_size, w.num_kv_heads, seed * 16 + 7)
+    vc, vs = W.fp8_pool(w.num_blocks, w.block_size, w.num_kv_heads, seed * 16 + 8)
+    return kc, vc, ks, vs
+
+
+def step_fp8(w, t, kc, vc, ks, vs):
+    """GPU store of the step's new tokens, then fp8 decode."""
+    sm = torch.from_numpy(w.slot_mapping).cuda()
+    pkv.store_kvcache_fp8(t["key"], t["value"], kc, vc, ks, vs, sm)
+    out = pkv.paged_decode_fp8(t["q"], kc, vc, ks, vs, torch.from_numpy(w.block_tables).cuda(),
+                               torch.from_numpy(w.context_lens).cuda(), w.scale)
+    torch.cuda.synchronize()
+    assert pkv.get_device_errors() == 0
+    return out
+
+
+def oracle_step_fp8(w, seq_ids, kc, vc, ks, vs, t):
+    """Oracle store + fp8 decode on host copies of the pool taken BEFORE the GPU step."""
+    k8, v8 = kc.cpu().numpy().copy(), vc.cpu().numpy().copy()
+    k_s, v_s = ks.cpu().numpy().copy(), vs.cpu().numpy().copy()
+    oracle.store_kvcache_fp8(bf16_to_u16(t["key"]), bf16_to_u16(t["value"]), k8, v8, k_s, v_s,
+                             w.slot_mapping, w.block_size)
+    mask = np.zeros(w.num_seqs, np.uint8)
+    mask[np.asarray(seq_ids)] = 1
+    out = oracle.paged_decode_fp8(bf16_to_u16(t["q"]), k8, v8, k_s, v_s, w.block_tables,
+                                  w.context_lens, w.scale, seq_mask=mask)
+    return out[np.asarray(seq_ids)], (k8, v8, k_s, v_s)
+
+
+@pytest.mark.parametrize("hkv,group,bs", [(8, 4, 16), (8, 1, 16), (8, 2, 32), (4, 8, 32),
+                                          (4, 2, 64), (8, 2, 256)])
+def test_fp8_store_and_decode_match_the_oracle(hkv, group, bs):
+    lens = [1, 2, 15, 16, 17, 0, 300, 1025, 77, 2000]
+    w = W.decode_workload(f"fp8_{hkv}x{group}_bs{bs}", lens, hkv * group, hkv, bs,
+                          seed=900 + hkv * 7 + group * 3 + bs)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    kc, vc, ks, vs = fp8_case(w, w.seed)
+    ids = np.arange(w.num_seqs)
+    ref, (k8, v8, k_s, v_s) = oracle_step_fp8(w, ids, kc, vc, ks, vs, t)
+    out = step_fp8(w, t, kc, vc, ks, vs)
+    # the store: codes and scales bit for bit, everywhere in the pool
+    assert np.array_equal(kc.cpu().numpy(), k8) and np.array_equal(vc.cpu().numpy(), v8)
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), k_s.view(np.uint32))
+    assert np.array_equal(vs.cpu().numpy().view(np.uint32), v_s.view(np.uint32))
+    assert_close(out, ref, w.name)
+    assert (out[5] == 0).all()
+
+
+def test_fp8_store_zero_and_large_rows():
+    w = W.decode_workload("fp8_rows", [3, 9], 32, 8, 16, seed=31)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    t["key"][0].zero_()                              # an all-zero row: codes 0, scale 0
+    t["value"][1] *= 1000.0                          # large values: scale grows, codes saturate at 448
+    kc, vc, ks, vs = fp8_case(w, 31)
+    ids = np.arange(w.num_seqs)
+    ref, (k8, v8, k_s, v_s) = oracle_step_fp8(w, ids, kc, vc, ks, vs, t)
+    out = step_fp8(w, t, kc, vc, ks, vs)
+    assert np.array_equal(kc.cpu().numpy(), k8) and np.array_equal(vc.cpu().numpy(), v8)
+    assert np.array_equal(ks.cpu().numpy(), k_s) and np.array_equal(vs.cpu().numpy(), v_s)
+    s0 = int(w.slot_mapping[0])
+    assert (kc.view(-1, 8, 128)[s0] == 0).all() and (ks[s0] == 0).all()
+    assert_close(out, ref, w.name)
+
+
+def test_fp8_decode_512seq_full_size_sampled():
+    w = W.decode_512seq(fill="device")
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    kc, vc, ks, vs = fp8_case(w, w.seed)
+    rng = np.random.default_rng(6)
+    ids = np.unique(np.concatenate([rng.choice(w.num_seqs, 16, replace=False),
+                                    [int(np.argmax(w.context_lens)), int(np.argmin(w.context_lens))]]))
+    ref, _ = oracle_step_fp8(w, ids, kc, vc, ks, vs, t)
+    out = step_fp8(w, t, kc, vc, ks, vs)
+    assert_close(out[torch.from_numpy(ids).cuda()], ref, w.name)
+
+
+def test_fp8_decode_rejects_shapes_without_the_kernel():
+    w = W.decode_workload("fp8_bad", [5, 9], 6, 2, 16, seed=32)     # Hkv 2: no fp8 kernel
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    kc, vc, ks, vs = fp8_case(w, 32)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_decode_fp8(t["q"], kc, vc, ks, vs, torch.from_numpy(w.block_tables).cuda(),
+                             torch.from_numpy(w.context_lens).cuda(), w.scale)
+    assert e.value.status == -2
