@@ -417,9 +417,131 @@ def run_pkv(args, rank, world, device):
     result["prefill_row"] = measure_prefill(args, device, steps=max(5, min(args.steps, 20)))
     result["gpu_launches_prefill_row"] = 2 * max(5, min(args.steps, 20))
     result["copy_blocks_row"] = measure_copy_blocks(device, steps=max(5, min(args.steps, 20)))
+    result["fp8_decode_row"] = measure_fp8_decode(device, steps=max(5, min(args.steps, 20)))
+    result["mixed_batch_row"] = measure_mixed(device, steps=max(5, min(args.steps, 20)))
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_oracle_sample(w)
     return result
+
+
+def fp8_decode_bytes(w) -> int:
+    """Algorithmic HBM bytes of one fp8 decode launch: one-byte K and V codes of
+    every cached token once per KV head plus their fp32 row scales, q in, out,
+    block-table entries and context lengths."""
+    ctx = w.context_lens.astype(np.int64)
+    kv = int((ctx * w.num_kv_heads * (w.head_dim + 4) * 2).sum())
+    qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * 2
+    tables = int((4 * ((ctx + w.block_size - 1) // w.block_size)).sum()) + 4 * w.num_seqs
+    return kv + qo + tables
+
+
+def measure_fp8_decode(device, steps):
+    """The fp8 KV row: the 512-sequence decode batch over an fp8 E4M3 cache
+    (per token-head scales): the quantizing store of the 512 new tokens, then
+    pkv_paged_decode_fp8, each timed with CUDA events."""
+    import torch
+    import paged_kv_cache_86_gb300 as pkv
+    from paged_kv_cache_86_gb300 import workloads as W
+    w = make_workload("decode_512seq", fill="device")
+    t = {k: v.to(device) for k, v in w.tensors.items() if k in ("q", "key", "value")}
+    kc, ks = W.fp8_pool(w.num_blocks, w.block_size, w.num_kv_heads, w.seed * 16 + 7, device=device)
+    vc, vs = W.fp8_pool(w.num_blocks, w.block_size, w.num_kv_heads, w.seed * 16 + 8, device=device)
+    bt = torch.from_numpy(w.block_tables).to(device)
+    cl = torch.from_numpy(w.context_lens).to(device)
+    sm = torch.from_numpy(w.slot_mapping).to(device)
+    out = torch.empty_like(t["q"])
+    ws = torch.empty(pkv.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def store():
+        pkv.store_kvcache_fp8(t["key"], t["value"], kc, vc, ks, vs, sm)
+
+    def decode():
+        pkv.paged_decode_fp8(t["q"], kc, vc, ks, vs, bt, cl, w.scale, out=out, workspace=ws)
+
+    for _ in range(3):
+        store()
+        decode()
+    torch.cuda.synchronize()
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    for a, b, c in evs:
+        a.record(stream)
+        store()
+        b.record(stream)
+        decode()
+        c.record(stream)
+    torch.cuda.synchronize()
+    if pkv.get_device_errors() != 0:
+        raise RuntimeError("device-side range check fired in the fp8 measurement")
+    store_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
+    decode_ms = statistics.mean(b.elapsed_time(c) for _, b, c in evs)
+    hpeak, _ = measured_peaks()
+    nbytes = fp8_decode_bytes(w)
+    step_ms = store_ms + decode_ms
+    return {"workload": w.name + "_fp8_e4m3", "decode_ms": decode_ms, "store_ms": store_ms,
+            "tokens_per_s": w.num_seqs / (step_ms * 1e-3),
+            "algorithmic_bytes_per_launch": nbytes,
+            "gbs": nbytes / (decode_ms * 1e-3) / 1e9,
+            "frac_of_hbm": nbytes / (decode_ms * 1e-3) / 1e9 / hpeak,
+            "l2": "inputs larger than L2 (1.2 GB of codes per launch)"}
+
+
+def measure_mixed(device, steps):
+    """The mixed-batch row: one round of 256 decode requests (lengths as the
+    512-sequence batch's distribution) and 8 prefill chunks of 512 after prefixes
+    U[0, 3584] -- 4352 scheduled tokens -- through pkv_mixed_step, and the same
+    round through pkv_store_kvcache + pkv_paged_prefill over every sequence."""
+    import torch
+    import paged_kv_cache_86_gb300 as pkv
+    from paged_kv_cache_86_gb300 import workloads as W
+    rng = np.random.default_rng(86011)
+    dec = np.clip(np.rint(np.exp(np.log(800) + rng.standard_normal(256))), 16, 4096).astype(int)
+    prefixes = rng.integers(0, 3585, 8)
+    q_lens = [1] * len(dec) + [512] * 8
+    w = W.prefill_workload("mixed_256decode_8x512chunks_bs16", q_lens,
+                           [int(n) - 1 for n in dec] + [int(x) for x in prefixes], 32, 8, 16,
+                           seed=86011, fill="device", device=device)
+    t = {k: v.to(device) for k, v in w.tensors.items()}
+    bt = torch.from_numpy(w.block_tables).to(device)
+    sm = torch.from_numpy(w.slot_mapping).to(device)
+    cq = torch.from_numpy(w.cu_seqlens_q).to(device)
+    ck = torch.from_numpy(w.cu_seqlens_k).to(device)
+    out = torch.empty_like(t["q"])
+    d = len(dec)
+    mq, mk = int(w.q_lens.max()), int(w.context_lens.max())
+    ws = torch.empty(max(pkv.mixed_workspace_size(d, 32, 8), 256), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def mixed():
+        pkv.mixed_step(t["q"], t["key"], t["value"], sm, t["k_cache"], t["v_cache"], cq, ck, bt, d,
+                       w.scale, mq, mk, out=out, workspace=ws)
+
+    def prefill_all():
+        pkv.store_kvcache(t["key"], t["value"], t["k_cache"], t["v_cache"], sm)
+        pkv.paged_prefill(t["q"], t["k_cache"], t["v_cache"], cq, ck, bt, w.scale, mq, mk, out=out)
+
+    res = {}
+    for name, fn in (("mixed_step", mixed), ("store_plus_prefill_kernel_for_all", prefill_all)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        res[name] = statistics.median(times)
+    if pkv.get_device_errors() != 0:
+        raise RuntimeError("device-side range check fired in the mixed-batch measurement")
+    tokens = int(w.num_q_rows)
+    return {"workload": w.name, "scheduled_tokens": tokens, "ms": res["mixed_step"],
+            "tokens_per_s": tokens / (res["mixed_step"] * 1e-3),
+            "ms_all_through_prefill_kernel": res["store_plus_prefill_kernel_for_all"],
+            "l2": "K/V of the round larger than L2 (~1 GB); median of launches"}
 
 
 def measure_copy_blocks(device, steps):

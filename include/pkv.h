@@ -15,7 +15,9 @@
  *                      token and the decode in one call);
  *   pkv_paged_prefill  varlen query chunks (cu_seqlens_q) over their cached
  *                      prefix plus themselves (cu_seqlens_k), causal;
- *   pkv_copy_blocks    copy-on-write of shared cache blocks.
+ *   pkv_copy_blocks    copy-on-write of shared cache blocks;
+ *   *_fp8              the store and the decode over an fp8 E4M3 cache;
+ *   pkv_mixed_step     a batch of decode requests and prefill chunks.
  *
  * Cache layout. One layer's K cache and V cache are two separate arrays of
  * shape [num_blocks, block_size, num_kv_heads, head_dim], row-major, bf16.
@@ -98,6 +100,91 @@ pkv_status pkv_store_kvcache(const void *key, const void *value,
                              int32_t block_size, int32_t num_blocks,
                              int64_t key_token_stride, int64_t value_token_stride,
                              pkv_dtype dtype, void *stream);
+
+/* ------------------------------------------------------------ mixed batch --
+ * pkv_mixed_step: one scheduling round's batch of decode requests and prefill
+ * chunks under one token budget, N_scheduled = N_decode + N_prefill_chunk
+ * (推理运行时 §Chunked prefill; §Prefill 与 decode 输入: the tokens of all
+ * requests are flattened into one array and per-sequence metadata gives each
+ * query range, context length and block table -- decode requests have one
+ * query, chunks several, with cached history).
+ *   Layout: sequences 0 .. num_decode_seqs-1 are decode requests, one query
+ *   row each, rows 0 .. num_decode_seqs-1 (the decode-first order of a batch
+ *   builder that gives every decode request its token before filling the rest
+ *   of the budget with prefill chunks); sequences num_decode_seqs .. num_seqs-1
+ *   are chunks. cu_seqlens_q / cu_seqlens_k [num_seqs + 1] as for
+ *   pkv_paged_prefill (bottom-right causal); key / value [total_q, Hkv, D] are
+ *   the K/V of every query row, written at slot_mapping [total_q] first.
+ *   max_seqlen_q / max_seqlen_k bound the chunks' query rows and every
+ *   sequence's keys.
+ *   workspace: at least pkv_mixed_workspace_size(num_decode_seqs, ...) bytes,
+ *   256-byte aligned.
+ * The result equals pkv_store_kvcache followed by pkv_paged_prefill over the
+ * whole batch; the decode sequences run on the split decode kernels instead of
+ * occupying a 128-row query tile each. A decode sequence with other than one
+ * query row sets PKV_DEVERR_LENGTH. Launches: store, decode (plan, attention,
+ * combine), prefill, in stream order.
+ */
+size_t pkv_mixed_workspace_size(int32_t num_decode_seqs, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_dim);
+
+pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void *value,
+                          const int32_t *slot_mapping,
+                          int64_t key_token_stride, int64_t value_token_stride,
+                          void *k_cache, void *v_cache,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                          int32_t max_seqlen_q, int32_t max_seqlen_k,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          int32_t num_seqs, int32_t num_decode_seqs, int32_t total_q,
+                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, int32_t num_blocks, float scale,
+                          void *workspace, size_t workspace_bytes,
+                          pkv_dtype dtype, void *stream);
+
+/* ---------------------------------------------------------------- fp8 KV --
+ * A quantized cache: the KV cache stores low-bit values instead of bf16, at
+ * some loss of accuracy (LLM Infra 101 v0.2, KV Quantization). Format: OCP FP8
+ * E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; largest
+ * magnitude 448; 0x7F / 0xFF are NaN) with one fp32 scale per (token, KV head)
+ * row of head_dim values, for K and V separately:
+ *   k_cache, v_cache    [num_blocks, block_size, num_kv_heads, 128] uint8 codes
+ *   k_scales, v_scales  [num_blocks * block_size, num_kv_heads] float, 16-byte
+ *                       aligned; the scale of slot s, head h is element
+ *                       s * num_kv_heads + h.
+ * A row's value d is e4m3(code_d) * scale.
+ *
+ * pkv_store_kvcache_fp8: like pkv_store_kvcache, but each new bf16 row x is
+ * quantized on the way: amax = max |x_d|; scale = amax / 448 and codes
+ * E4M3(x_d * (448 / amax)), both fp32 operations rounded to nearest even, the
+ * code rounded to the nearest finite E4M3 value (ties to even) and saturated
+ * at 448; an all-zero row stores zero codes and scale 0. head_dim 128.
+ */
+pkv_status pkv_store_kvcache_fp8(const void *key, const void *value,
+                                 void *k_cache, void *v_cache,
+                                 float *k_scales, float *v_scales,
+                                 const int32_t *slot_mapping, int32_t num_tokens,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 int32_t num_blocks,
+                                 int64_t key_token_stride, int64_t value_token_stride,
+                                 void *stream);
+
+/* pkv_paged_decode_fp8: pkv_paged_decode over fp8 caches -- the attention of
+ * each q row over the dequantized K/V rows. Same arguments, workspace and
+ * errors as pkv_paged_decode, plus the scale arrays. q and out stay bf16; q
+ * enters the tensor core as f16 (exact for |q| in the normal f16 range, up to
+ * 65504). Supported: head_dim 128, num_kv_heads 4 or 8, num_q_heads /
+ * num_kv_heads in {1, 2, 4, 8} with num_q_heads <= 32, block_size a multiple
+ * of 128 / num_kv_heads; other shapes return PKV_ERR_SHAPE.
+ */
+pkv_status pkv_paged_decode_fp8(void *out, const void *q,
+                                const void *k_cache, const void *v_cache,
+                                const float *k_scales, const float *v_scales,
+                                const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                const int32_t *context_lens, int32_t num_seqs,
+                                int32_t max_context_len,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t block_size, int32_t num_blocks, float scale,
+                                void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------ block copy --
  * pkv_copy_blocks: for p < num_pairs, rows 0 .. num_rows[p]-1 of physical block

@@ -63,6 +63,11 @@ def load(path: str = LIB_PATH):
                                               i64, i64, vp]
         lib.pkv_paged_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
                                              i32, i32, i32, i32, f32, vp, sz, vp]
+        lib.pkv_mixed_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.pkv_mixed_workspace_size.restype = sz
+        lib.pkv_mixed_step.argtypes = [vp, vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, i32, i32, vp,
+                                       i32, i32, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz,
+                                       ctypes.c_int, vp]
         lib.pkv_copy_blocks.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int,
                                         vp]
         lib.pkv_prefill_workspace_size.argtypes = [i32, i32, i32, i32]
@@ -76,7 +81,7 @@ def load(path: str = LIB_PATH):
         lib.pkv_version.restype = i32
         for name in ("pkv_store_kvcache", "pkv_paged_decode", "pkv_decode_step",
                      "pkv_paged_prefill", "pkv_copy_blocks", "pkv_store_kvcache_fp8",
-                     "pkv_paged_decode_fp8", "pkv_get_device_errors"):
+                     "pkv_paged_decode_fp8", "pkv_mixed_step", "pkv_get_device_errors"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -198,6 +203,53 @@ def paged_decode_fp8(q, k_cache, v_cache, k_scales, v_scales, block_tables, cont
                                     float(scale), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(),
                                     _stream(q, stream)), "pkv_paged_decode_fp8")
+    return out
+
+
+def mixed_workspace_size(num_decode_seqs: int, num_q_heads: int, num_kv_heads: int,
+                         head_dim: int = 128) -> int:
+    return int(load().pkv_mixed_workspace_size(num_decode_seqs, num_q_heads, num_kv_heads,
+                                               head_dim))
+
+
+def mixed_step(q, key, value, slot_mapping, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+               block_tables, num_decode_seqs: int, scale: float, max_seqlen_q: int,
+               max_seqlen_k: int, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """One mixed round: sequences [0, num_decode_seqs) are decode requests with one
+    query row each (rows 0..D-1), the rest prefill chunks; every query row's K/V
+    (key / value [total_q, Hkv, D]) is stored at slot_mapping first. Returns out
+    [total_q, Hq, D] bf16."""
+    lib = load()
+    _need(q, "q", torch.bfloat16, 3)
+    for t, n in ((key, "key"), (value, "value")):
+        _need(t, n, torch.bfloat16, 3)
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{n} rows must be contiguous [Hkv, D] blocks")
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, n, torch.bfloat16, 4)
+    for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k"),
+                 (slot_mapping, "slot_mapping")):
+        _need(t, n, torch.int32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    total_q, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    s = cu_seqlens_q.shape[0] - 1
+    if (cu_seqlens_k.shape[0] != s + 1 or block_tables.shape[0] != s
+            or slot_mapping.shape[0] != total_q or key.shape != (total_q, hkv, d)
+            or value.shape != (total_q, hkv, d)):
+        raise ValueError("metadata shape mismatch")
+    if out is None:
+        out = torch.empty_like(q)
+    need = mixed_workspace_size(num_decode_seqs, hq, hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(lib.pkv_mixed_step(_ptr(out), _ptr(q), _ptr(key), _ptr(value), _ptr(slot_mapping),
+                              key.stride(0), value.stride(0), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_seqlen_q),
+                              int(max_seqlen_k), _ptr(block_tables), block_tables.shape[1], s,
+                              int(num_decode_seqs), total_q, hq, hkv, d, bs, nb, float(scale),
+                              _ptr(workspace), workspace.numel() * workspace.element_size(),
+                              PKV_BF16, _stream(q, stream)), "pkv_mixed_step")
     return out
 
 

@@ -265,6 +265,121 @@ pkv_status pkv_decode_step(void *out, const void *q, const void *key_new, const 
                      num_blocks, scale, workspace, workspace_bytes, dtype, stream);
 }
 
+size_t pkv_mixed_workspace_size(int32_t num_decode_seqs, int32_t num_q_heads,
+                                int32_t num_kv_heads, int32_t head_dim) {
+  if (num_decode_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim != 128 ||
+      num_q_heads % num_kv_heads != 0)
+    return 0;
+  const size_t lens = (sizeof(int32_t) * (size_t(num_decode_seqs) + 1) + 255) & ~size_t(255);
+  if (num_decode_seqs == 0) return lens;
+  cudaError_t e;
+  const size_t dec = pkv::decode_workspace_upper_bound(num_decode_seqs, num_q_heads, num_kv_heads, &e);
+  return dec == 0 ? 0 : lens + dec;
+}
+
+pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void *value,
+                          const int32_t *slot_mapping, int64_t key_token_stride,
+                          int64_t value_token_stride, void *k_cache, void *v_cache,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                          int32_t max_seqlen_q, int32_t max_seqlen_k,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          int32_t num_seqs, int32_t num_decode_seqs, int32_t total_q,
+                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, int32_t num_blocks, float scale, void *workspace,
+                          size_t workspace_bytes, pkv_dtype dtype, void *stream) {
+  if (dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (num_seqs < 0 || num_decode_seqs < 0 || num_decode_seqs > num_seqs || total_q < 0 ||
+      num_q_heads < 1 || num_kv_heads < 1 || block_size < 1 || num_blocks < 1 ||
+      max_blocks_per_seq < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || !std::isfinite(scale))
+    return PKV_ERR_ARG;
+  if (head_dim != 128) return PKV_ERR_SHAPE;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_SHAPE;
+  if (int64_t(max_seqlen_k) > int64_t(max_blocks_per_seq) * block_size) return PKV_ERR_ARG;
+  if (total_q < num_decode_seqs || num_seqs - num_decode_seqs > 65535) return PKV_ERR_ARG;
+  if (num_seqs == 0 || total_q == 0) return PKV_OK;
+  if (!out || !q || !key || !value || !slot_mapping || !k_cache || !v_cache || !cu_seqlens_q ||
+      !cu_seqlens_k || !block_tables || !workspace)
+    return PKV_ERR_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(key) || !aligned16(value) ||
+      !aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PKV_ERR_ARG;
+  const int64_t row = int64_t(num_kv_heads) * head_dim;
+  if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 != 0 ||
+      value_token_stride % 8 != 0)
+    return PKV_ERR_ARG;
+  const int num_prefill = num_seqs - num_decode_seqs;
+  if (num_prefill > 0 && !pkv::prefill_supported(num_q_heads, num_kv_heads, block_size))
+    return PKV_ERR_SHAPE;
+  cudaError_t e;
+  pkv::DecodePlan plan{};
+  if (num_decode_seqs > 0 &&
+      !pkv::choose_decode_plan(num_q_heads, num_kv_heads, block_size, &plan, &e))
+    return e != cudaSuccess ? PKV_ERR_CUDA : PKV_ERR_SHAPE;
+  const size_t lens_bytes = (sizeof(int32_t) * (size_t(num_decode_seqs) + 1) + 255) & ~size_t(255);
+  const size_t dec_bytes = num_decode_seqs > 0
+      ? pkv::decode_workspace_bytes(num_decode_seqs, num_q_heads, num_kv_heads, plan) : 0;
+  if (workspace_bytes < lens_bytes + dec_bytes) return PKV_ERR_WORKSPACE;
+  uint32_t *err = pkv::device_error_word(&e);
+  if (!err) return PKV_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // 1. every new token of the batch (decode tokens and chunk tokens) into the cache
+  e = pkv::launch_store_kvcache(key, value, k_cache, v_cache, slot_mapping, total_q,
+                                static_cast<int32_t>(row), key_token_stride, value_token_stride,
+                                int64_t(num_blocks) * block_size, err, st);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+  // 2. the decode sequences 0..D-1 (one query row each, rows 0..D-1)
+  if (num_decode_seqs > 0) {
+    int32_t *lens = static_cast<int32_t *>(workspace);
+    if ((e = pkv::launch_mixed_decode_lens(cu_seqlens_q, cu_seqlens_k, num_decode_seqs, lens, err,
+                                           st)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    pkv::DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.context_lens = lens;
+    a.num_seqs = num_decode_seqs;
+    a.max_context_len = max_seqlen_k;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.workspace = static_cast<uint8_t *>(workspace) + lens_bytes;
+    a.workspace_bytes = dec_bytes;
+    a.err = err;
+    if ((e = pkv::launch_paged_decode(a, plan, st)) != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  // 3. the prefill chunks D..S-1 (their query rows are absolute offsets in cu_seqlens_q)
+  if (num_prefill > 0) {
+    pkv::PrefillArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.cu_seqlens_q = cu_seqlens_q + num_decode_seqs;
+    a.cu_seqlens_k = cu_seqlens_k + num_decode_seqs;
+    a.max_seqlen_q = max_seqlen_q;
+    a.max_seqlen_k = max_seqlen_k;
+    a.block_tables = block_tables + static_cast<int64_t>(num_decode_seqs) * max_blocks_per_seq;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_seqs = num_prefill;
+    a.total_q = total_q;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.causal = 1;
+    a.err = err;
+    if ((e = pkv::launch_paged_prefill(a, st)) != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
 size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num_q_heads,
                                   int32_t head_dim) {
   (void)num_seqs;

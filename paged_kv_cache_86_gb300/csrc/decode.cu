@@ -690,6 +690,27 @@ int split_grid(int num_q_heads, int num_kv_heads, cudaError_t *status) {
   return per_sm * sm_count(dev);
 }
 
+// Mixed batch: sequences 0..D-1 are decode sequences (one query row each, rows
+// 0..D-1); their context lengths are the differences of cu_seqlens_k. A layout
+// that breaks this (a decode sequence with other than one query row) is
+// reported as PKV_DEVERR_LENGTH.
+__global__ void mixed_decode_lens_kernel(const int32_t *__restrict__ cu_q,
+                                         const int32_t *__restrict__ cu_k, int num_decode,
+                                         int32_t *__restrict__ lens, uint32_t *err) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= num_decode) return;
+  lens[i] = cu_k[i + 1] - cu_k[i];
+  if (cu_q[i] != i || cu_q[i + 1] != i + 1) raise_error(err, PKV_DEVERR_LENGTH);
+}
+
+cudaError_t launch_mixed_decode_lens(const int32_t *cu_q, const int32_t *cu_k, int num_decode,
+                                     int32_t *lens, uint32_t *err, cudaStream_t stream) {
+  if (num_decode == 0) return cudaSuccess;
+  mixed_decode_lens_kernel<<<(num_decode + 255) / 256, 256, 0, stream>>>(cu_q, cu_k, num_decode,
+                                                                         lens, err);
+  return cudaGetLastError();
+}
+
 // The plan launch: CTA 0 plans the ranges; with new tokens (decode step), CTAs
 // 1.. write them, 32 sequences per CTA.
 cudaError_t launch_plan(const DecodeArgs &a, int grid, int units_per_token, int min_range,

@@ -68,6 +68,11 @@ struct DecodeArgs {
   const float *v_scales = nullptr;
 };
 
+// Context lengths of the decode sequences 0..D-1 of a mixed batch from
+// cu_seqlens_k (checks that each has exactly one query row).
+cudaError_t launch_mixed_decode_lens(const int32_t *cu_q, const int32_t *cu_k, int num_decode,
+                                     int32_t *lens, uint32_t *err, cudaStream_t stream);
+
 // Which decode kernel runs and on how many CTAs. Block sizes that are a
 // multiple of 8 (and at most 16 query heads per KV head) run the tcgen05
 // kernel; other shapes the CUDA-core split kernel.

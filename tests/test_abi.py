@@ -100,3 +100,40 @@ def test_copy_blocks_host_validation_needs_no_gpu(lib):
     assert lib.pkv_copy_blocks(a, a, null, a, null, 3, 8, 128, 16, 64, 0, null) == -1  # no src
     assert lib.pkv_copy_blocks(vp(264), a, a, a, null, 3, 8, 128, 16, 64, 0, null) == -1  # align
     assert lib.pkv_copy_blocks(null, null, null, null, null, 0, 8, 128, 16, 64, 0, null) == 0
+
+
+def test_fp8_host_validation_needs_no_gpu(lib):
+    vp, null = ctypes.c_void_p, ctypes.c_void_p(0)
+    a = vp(256)
+    # store: head_dim other than 128, null scales, misaligned scales, short stride
+    assert lib.pkv_store_kvcache_fp8(a, a, a, a, a, a, a, 3, 8, 64, 16, 8, 1024, 1024, null) == -2
+    assert lib.pkv_store_kvcache_fp8(a, a, a, a, null, a, a, 3, 8, 128, 16, 8, 1024, 1024, null) == -1
+    assert lib.pkv_store_kvcache_fp8(a, a, a, a, vp(260), a, a, 3, 8, 128, 16, 8, 1024, 1024, null) == -1
+    assert lib.pkv_store_kvcache_fp8(a, a, a, a, a, a, a, 3, 8, 128, 16, 8, 512, 1024, null) == -1
+    assert lib.pkv_store_kvcache_fp8(null, null, null, null, null, null, null, 0, 8, 128, 16, 8,
+                                     1024, 1024, null) == 0
+    # decode: missing scales, head_dim, no sequences
+    assert lib.pkv_paged_decode_fp8(a, a, a, a, null, a, a, 4, a, 2, 64, 32, 8, 128, 16, 8, 0.1,
+                                    a, 1 << 20, null) == -1
+    assert lib.pkv_paged_decode_fp8(a, a, a, a, a, a, a, 4, a, 2, 64, 32, 8, 64, 16, 8, 0.1,
+                                    a, 1 << 20, null) == -2
+    assert lib.pkv_paged_decode_fp8(null, null, null, null, null, null, null, 4, null, 0, 64, 32,
+                                    8, 128, 16, 8, 0.1, null, 0, null) == 0
+
+
+def test_mixed_step_host_validation_needs_no_gpu(lib):
+    vp, null = ctypes.c_void_p, ctypes.c_void_p(0)
+    a = vp(256)
+
+    def step(num_seqs=4, num_decode=2, total_q=10, head_dim=128, dtype=0, ws=a, ks=1024):
+        return lib.pkv_mixed_step(a, a, a, a, a, ks, 1024, a, a, a, a, 8, 64, a, 4, num_seqs,
+                                  num_decode, total_q, 32, 8, head_dim, 16, 8, 0.1, ws, 1 << 20,
+                                  dtype, null)
+
+    assert step(dtype=7) == -3
+    assert step(num_decode=5) == -1            # more decode sequences than sequences
+    assert step(total_q=1) == -1               # fewer rows than decode sequences
+    assert step(head_dim=64) == -2
+    assert step(ws=null) == -1
+    assert step(ks=100) == -1                  # key stride shorter than a row
+    assert step(num_seqs=0, num_decode=0, total_q=0) == 0

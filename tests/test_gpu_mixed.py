@@ -1,0 +1,84 @@
+"""GPU parity of pkv_mixed_step (decode requests and prefill chunks of one
+round, decode first) against the oracle's store + prefill over the whole
+flattened batch, and of its decode rows against pkv_paged_decode."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_86_gb300 as pkv
+from paged_kv_cache_86_gb300 import workloads as W
+from pkv_testutil import assert_close, device_meta, prefill_step_reference
+
+pytestmark = pytest.mark.gpu
+
+
+def mixed_workload(name, decode_lens, chunk_q, chunk_prefix, hq, hkv, bs, seed):
+    """Decode sequences first (one query row at position len - 1), then chunks."""
+    q_lens = [1] * len(decode_lens) + list(chunk_q)
+    prefixes = [n - 1 for n in decode_lens] + list(chunk_prefix)
+    return W.prefill_workload(name, q_lens, prefixes, hq, hkv, bs, seed), len(decode_lens)
+
+
+def run_mixed(w, d, t):
+    m = device_meta(w)
+    out = pkv.mixed_step(t["q"], t["key"], t["value"], m["slot_mapping"], t["k_cache"], t["v_cache"],
+                         m["cu_seqlens_q"], m["cu_seqlens_k"], m["block_tables"], d, w.scale,
+                         max_seqlen_q=int(w.q_lens.max()), max_seqlen_k=int(w.context_lens.max()))
+    torch.cuda.synchronize()
+    return out, m
+
+
+@pytest.mark.parametrize("hkv,group,bs", [(8, 4, 16), (2, 4, 16), (8, 2, 32), (4, 3, 16)])
+def test_mixed_step_matches_the_oracle(hkv, group, bs):
+    w, d = mixed_workload(f"mixed_{hkv}x{group}_bs{bs}", [1, 2, 17, 300, 1000], [3, 130, 64],
+                          [0, 70, 500], hkv * group, hkv, bs, seed=400 + hkv + group + bs)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    ref = prefill_step_reference(w, t["k_cache"], t["v_cache"], t["q"], t["key"], t["value"])
+    out, m = run_mixed(w, d, t)
+    assert pkv.get_device_errors() == 0
+    assert_close(out, ref, w.name)
+    # the decode rows came from the decode path: identical to pkv_paged_decode
+    # on the same (already stored) cache
+    lens = (m["cu_seqlens_k"][1:d + 1] - m["cu_seqlens_k"][:d]).contiguous()
+    dec = pkv.paged_decode(t["q"][:d].contiguous(), t["k_cache"], t["v_cache"],
+                           m["block_tables"][:d].contiguous(), lens, w.scale,
+                           max_context_len=int(w.context_lens.max()))
+    assert torch.equal(out[:d], dec)
+
+
+def test_mixed_step_only_decodes_and_only_chunks():
+    for dl, cq, cp in (([5, 40, 9], [], []), ([], [7, 129], [3, 0])):
+        w, d = mixed_workload("mixed_edge", dl, cq, cp, 16, 4, 16, seed=11)
+        t = {k: v.cuda() for k, v in w.tensors.items()}
+        ref = prefill_step_reference(w, t["k_cache"], t["v_cache"], t["q"], t["key"], t["value"])
+        out, _ = run_mixed(w, d, t)
+        assert pkv.get_device_errors() == 0
+        assert_close(out, ref, "mixed_edge")
+
+
+def test_mixed_step_flags_a_decode_sequence_with_two_rows():
+    w, d = mixed_workload("mixed_bad", [5, 9], [4], [2], 8, 2, 16, seed=12)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    # claim three decode sequences: the third one has four query rows
+    m = device_meta(w)
+    pkv.mixed_step(t["q"], t["key"], t["value"], m["slot_mapping"], t["k_cache"], t["v_cache"],
+                   m["cu_seqlens_q"], m["cu_seqlens_k"], m["block_tables"], 3, w.scale,
+                   max_seqlen_q=4, max_seqlen_k=int(w.context_lens.max()))
+    torch.cuda.synchronize()
+    assert pkv.get_device_errors() & pkv._lib.DEVERR_LENGTH
+
+
+def test_mixed_step_full_size_sampled():
+    rng = np.random.default_rng(13)
+    dec = np.clip(np.rint(np.exp(np.log(800) + rng.standard_normal(256))), 16, 4096).astype(int)
+    w, d = mixed_workload("mixed_256d_8x512", dec.tolist(), [512] * 8,
+                          rng.integers(0, 3585, 8).tolist(), 32, 8, 16, seed=14)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    mask = np.zeros(w.num_q_rows, np.uint8)
+    rows = np.concatenate([rng.choice(d, 12, replace=False), d + rng.choice(w.num_q_rows - d, 40, replace=False)])
+    mask[rows] = 1
+    ref = prefill_step_reference(w, t["k_cache"], t["v_cache"], t["q"], t["key"], t["value"], row_mask=mask)
+    out, _ = run_mixed(w, d, t)
+    assert pkv.get_device_errors() == 0
+    sel = np.sort(rows)
+    assert_close(out[torch.from_numpy(sel).cuda()], ref[sel], w.name)
