@@ -57,6 +57,7 @@ constexpr int kThreads = 224;  // K producer, MMA, 4 softmax warps, V producer
 constexpr int kThreadsF8 = 480;
 constexpr int kRawCodes = 16384;      // one fp8 stage: 128 rows x 128 one-byte codes
 constexpr int kRawStage = 17408;      // codes + 128 fp32 row scales, padded to 1024 B
+constexpr uint32_t kK0 = 128;         // fp8: first TMEM column of the f16 K stages (64 each)
 constexpr int kMaxN = 128;
 constexpr int kMaxG = 16;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -99,16 +100,17 @@ struct GLayout {
 __host__ __device__ inline GLayout g_layout(int stages, int n_cols, bool f8 = false) {
   GLayout L;
   const int small = n_cols * 128;         // one 64-dim half of Q^T / P^T (N rows x 128 B)
+  // fp8: the f16 K operand lives in TMEM, so shared memory holds only the V ring
   L.k = 0;
-  L.v = stages * kKVBytes;
-  L.q = 2 * stages * kKVBytes;            // two Q^T buffers (2 halves each)
-  L.p = L.q + 2 * 2 * small;              // P^T (2 halves over the 128 rows)
-  L.alpha = L.p + 2 * small;              // [2][kMaxN] rescale factors, [2] stage flags
+  L.v = f8 ? 0 : stages * kKVBytes;
+  L.q = L.v + stages * kKVBytes;
+  L.p = L.q + 2 * small;                  // one Q^T buffer (2 halves)
+  L.alpha = L.p + 2 * 2 * small;          // two P^T buffers (2 halves over the 128 rows each)
   L.lsum = L.alpha + (2 * kMaxN + 4) * 4; // [kMaxN] row sums
   L.msum = L.lsum + kMaxN * 4;            // [kMaxN] maxima
   L.desc = L.msum + kMaxN * 4;
   L.bar = L.desc + 4 * 32;
-  L.vflag = L.bar + 32 * 8 + 16;          // 32 barriers, TMEM slot + abort flag, then V stage flags
+  L.vflag = L.bar + 34 * 8 + 16;          // 34 barriers, TMEM slot + abort flag, then V stage flags
   L.total = L.vflag + 16;
   L.kr = L.vr = 0;
   if (f8) {                               // raw fp8 rings, 1024-aligned for the 128-byte swizzle
@@ -277,8 +279,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   auto v_empty = [&](int s) { return bar0 + 8u * (20 + s); };
   auto s_full = [&](int b) { return bar0 + 8u * (8 + b); };
   auto s_free = [&](int b) { return bar0 + 8u * (10 + b); };
-  const uint32_t p_full = bar0 + 8u * 12;
-  const uint32_t pv_done = bar0 + 8u * 13;
+  // P^T is double-buffered: stage j writes buffer j & 1, so the softmax of stage
+  // j only waits for PV(j-2) before writing, not for PV(j-1)
+  auto p_full = [&](int b) { return bar0 + 8u * (b ? 33 : 12); };
+  auto pv_done = [&](int b) { return bar0 + 8u * (b ? 32 : 13); };
   const uint32_t x_bar = bar0 + 8u * 14;    // per-stage exchange among the softmax warps
   const uint32_t l_bar = bar0 + 8u * 15;    // per-segment row-sum exchange
   // fp8: the loaders' copies land on kr_full / vr_full; the converters then
@@ -286,7 +290,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   auto kr_full = [&](int s) { return bar0 + 8u * (24 + s); };
   auto vr_full = [&](int s) { return bar0 + 8u * (28 + s); };
   volatile int *vflag = reinterpret_cast<volatile int *>(smem + L.vflag);  // V stage flags
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bar + 32 * 8);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.bar + 34 * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   GDesc *desc = reinterpret_cast<GDesc *>(smem + L.desc);
   float *alpha_buf = reinterpret_cast<float *>(smem + L.alpha);          // [2][kMaxN]
@@ -314,8 +318,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(s_full(b), 1);
       mbar_init(s_free(b), 4);
     }
-    mbar_init(p_full, 4);
-    mbar_init(pv_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(p_full(b), 4);
+      mbar_init(pv_done(b), 1);
+    }
     mbar_init(x_bar, 4);
     mbar_init(l_bar, 4);
     *abort_flag = 0;
@@ -425,7 +431,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         d.p1 = min(hi, c1) - c0;
         const bool complete = c0 >= lo && c1 <= hi;
         d.slot = complete ? -1 : (c0 <= lo ? 2 * int(blockIdx.x) : 2 * int(blockIdx.x) + 1);
-        d.qbuf = segs & 1;
+        d.qbuf = 0;  // one Q^T buffer: refilled once the previous segment's S MMAs are done
         d.pad = 0;
         const int32_t *row = p.block_tables + static_cast<size_t>(i) * p.max_blocks_per_seq;
         int cached = -(1 << 30), my_id = -1;
@@ -473,44 +479,71 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const uint32_t idesc_pv = (umma_idesc_bf16(kHD, N, false) | (1u << 15)) & kFmt;  // A (V) MN-major
       bool ok = true;
       int pv_issued = 0, s_issued = 0;
-      int prev_s = 0, prev_first = 0;
-      auto issue_pv = [&](int t, int s, int first) -> bool {
-        if (!mbar_wait(v_full(s), (t / S) & 1, abort_flag)) return false;
-        if (!mbar_wait(p_full, t & 1, abort_flag)) return false;
-        tc_fence_after();
+      // S(j) and PV(j-1) are independent (S^T is double-buffered, PV reads P^T and
+      // V), so each is issued as soon as its own inputs are ready: S(j) when K(j)
+      // has landed and S^T[j & 1] is free, PV(t) when P(t) and V(t) are ready.
+      // The issuer polls both without blocking on either.
+      uint8_t first_of[8];        // kFirst of stage t, kept from S(t) until PV(t)
+      int end_at = -1;            // index of the stage that ends the walk
+      unsigned long long idle_since = global_timer_ns();
+      for (uint32_t idle = 0;;) {
+        bool did = false;
+        if (end_at < 0 && s_issued - pv_issued < 4) {
+          const int j = s_issued, s = j % S, buf = j & 1;
+          if (mbar_test_wait(k_full(s), (j / S) & 1) &&
+              (j < 2 || mbar_test_wait(s_free(buf), ((j - 2) >> 1) & 1))) {
+            const GDesc d = desc[s];
+            if (d.flags & kEnd) {
+              end_at = j;
+            } else {
+              tc_fence_after();
+              const uint32_t q = sQ + d.qbuf * 2 * small;
 #pragma unroll
-        for (int kk = 0; kk < kRows / 16; ++kk)
-          umma_bf16(tmem_o, desc_v(sV + s * kKVBytes, kk), desc_k(sP, kk, small), idesc_pv,
-                    (first && kk == 0) ? 0u : 1u);
-        umma_commit(pv_done);
-        umma_commit(v_empty(s));
-        ++pv_issued;
-        return true;
-      };
-      for (int j = 0;; ++j) {
-        const int s = j % S;
-        if (!mbar_wait(k_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
-        const GDesc d = desc[s];
-        if (d.flags & kEnd) break;
-        const int buf = j & 1;
-        if (j >= 2 && !mbar_wait(s_free(buf), ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t q = sQ + d.qbuf * 2 * small;
+              for (int kk = 0; kk < kHD / 16; ++kk) {
+                if (F8)
+                  umma_tmem_a(tmem_s(buf), tmem + kK0 + s * 64 + kk * 8, desc_k(q, kk, small), idesc_s,
+                              kk > 0 ? 1u : 0u);
+                else
+                  umma_bf16(tmem_s(buf), desc_k(sK + s * kKVBytes, kk, kRegion), desc_k(q, kk, small),
+                            idesc_s, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(s_full(buf));
+              umma_commit(k_empty(s));
+              first_of[j & 7] = (d.flags & kFirst) ? 1 : 0;
+              ++s_issued;
+            }
+            did = true;
+          }
+        }
+        if (pv_issued < s_issued) {
+          const int t = pv_issued, s = t % S;
+          if (mbar_test_wait(v_full(s), (t / S) & 1) && mbar_test_wait(p_full(t & 1), (t >> 1) & 1)) {
+            tc_fence_after();
+            const bool first = first_of[t & 7] != 0;
 #pragma unroll
-        for (int kk = 0; kk < kHD / 16; ++kk)
-          umma_bf16(tmem_s(buf), desc_k(sK + s * kKVBytes, kk, kRegion), desc_k(q, kk, small),
-                    idesc_s, kk > 0 ? 1u : 0u);
-        umma_commit(s_full(buf));
-        umma_commit(k_empty(s));
-        ++s_issued;
-        if (j > 0 && !issue_pv(j - 1, prev_s, prev_first)) { ok = false; break; }
-        prev_s = s;
-        prev_first = (d.flags & kFirst) ? 1 : 0;
+            for (int kk = 0; kk < kRows / 16; ++kk)
+              umma_bf16(tmem_o, desc_v(sV + s * kKVBytes, kk), desc_k(sP + (t & 1) * 2 * small, kk, small),
+                        idesc_pv, (first && kk == 0) ? 0u : 1u);
+            umma_commit(pv_done(t & 1));
+            umma_commit(v_empty(s));
+            ++pv_issued;
+            did = true;
+          }
+        }
+        if (end_at >= 0 && pv_issued == s_issued) break;
+        if (did) {
+          idle = 0;
+          idle_since = global_timer_ns();
+        } else if ((++idle & 255u) == 0) {
+          if (*abort_flag || global_timer_ns() - idle_since > kWaitTimeoutNs) {
+            ok = false;
+            break;
+          }
+        }
       }
-      if (ok && s_issued > pv_issued) ok = issue_pv(s_issued - 1, prev_s, prev_first);
       if (!ok) fail();
       if (s_issued > 0) mbar_wait(s_full((s_issued - 1) & 1), ((s_issued - 1) >> 1) & 1, nullptr);
-      if (pv_issued > 0) mbar_wait(pv_done, (pv_issued - 1) & 1, nullptr);
+      if (pv_issued > 0) mbar_wait(pv_done((pv_issued - 1) & 1), ((pv_issued - 1) >> 1) & 1, nullptr);
     }
     __syncwarp();
   } else if (F8 && warp >= 7) {
@@ -519,7 +552,8 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // 128-code row per thread, from E4M3 into the f16 operand layout (and, at
     // a segment's first stage, the new Q^T buffer from bf16 to f16 in place).
     const bool is_k = warp < 11;
-    const int r = static_cast<int>(threadIdx.x) - (is_k ? 224 : 352);
+    // K rows go to TMEM, where a warp reaches only its lane quadrant (warp % 4)
+    const int r = is_k ? (warp & 3) * 32 + lane : static_cast<int>(threadIdx.x) - 352;
     for (int j = 0;; ++j) {
       const int s = j % S;
       if (!warp_wait(is_k ? kr_full(s) : vr_full(s), (j / S) & 1, abort_flag)) {
@@ -532,8 +566,34 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (is_k && lane == 0) mbar_arrive(k_full(s));  // lets the MMA and softmax see the end
         break;
       }
-      convert_row_e4m3(base + (is_k ? L.kr : L.vr) + s * kRawStage,
-                       (is_k ? sK : sV) + s * kKVBytes, r);
+      if (is_k) {
+        // row r of the raw K stage -> TMEM lane r, columns kK0 + 64 s .. +63 (f16 pairs)
+        const uint32_t raw = base + L.kr + s * kRawStage + r * 128;
+        const uint32_t sw = static_cast<uint32_t>(r & 7);
+        float words[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 w = lds128(raw + (((4 * h + c) ^ sw) << 4));
+            const uint4 lo = e4m3x8_to_f16x8(make_uint2(w.x, w.y));
+            const uint4 hi = e4m3x8_to_f16x8(make_uint2(w.z, w.w));
+            words[8 * c + 0] = __uint_as_float(lo.x);
+            words[8 * c + 1] = __uint_as_float(lo.y);
+            words[8 * c + 2] = __uint_as_float(lo.z);
+            words[8 * c + 3] = __uint_as_float(lo.w);
+            words[8 * c + 4] = __uint_as_float(hi.x);
+            words[8 * c + 5] = __uint_as_float(hi.y);
+            words[8 * c + 6] = __uint_as_float(hi.z);
+            words[8 * c + 7] = __uint_as_float(hi.w);
+          }
+          tmem_st32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kK0 + s * 64 + h * 32, words);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+      } else {
+        convert_row_e4m3(base + L.vr + s * kRawStage, sV + s * kKVBytes, r);
+      }
       if (is_k && (flags & kFirst)) {
         const uint32_t qbuf = sQ + desc[s].qbuf * 2 * small;
         for (int i = r; i < static_cast<int>(small) / 8; i += 128) {  // 2 * small bytes, 16 per chunk
@@ -567,7 +627,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     int segs_done = 0;
     bool ok = true;
     // P^T (N rows x 128 stage rows, K-major, 128-byte swizzle): element (n, r)
-    const uint32_t p_region = sP + (r >> 6) * small;
+    const uint32_t p_half = (r >> 6) * small;
     const int rc = r & 63;
     for (int j = 0;; ++j) {
       const int s = j % S;
@@ -634,11 +694,12 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         pr[g] = valid ? ex2(sc[g] - m_used[g]) : 0.f;
         l_part[g] = first ? pr[g] : l_part[g] * alpha[g] + pr[g];
       }
-      // the previous PV must be done before P^T is rewritten or O^T rescaled
-      if (j > 0) {
-        if (!warp_wait(pv_done, (j - 1) & 1, abort_flag)) { ok = false; break; }
+      // PV(j-2) read this stage's P^T buffer: it must be done before the rewrite
+      if (j >= 2) {
+        if (!warp_wait(pv_done(j & 1), ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
       }
+      const uint32_t p_region = sP + (j & 1) * 2 * small + p_half;
       const bool partial = d.pa < d.p0 || d.pa + T > d.p1;
       // fp8: P^T rows carry the V row scale, read from the raw V stage
       if ((F8 || partial) && !warp_wait(v_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
@@ -671,6 +732,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (lane == 0) mbar_arrive(x_bar);
       if (!warp_wait(x_bar, j & 1, abort_flag)) { ok = false; break; }
       if (grow_flag[j & 1] == j + 1) {
+        // O^T may only be rescaled once every earlier PV has landed in it
+        if (j >= 1) {
+          if (!warp_wait(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+        }
         for (int c0 = 0; c0 < N; c0 += 16) {
           float o[16];
           tmem_ld16(tmem_o + lane_off + c0, o);
@@ -691,7 +757,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full(j & 1));
 
       if (d.flags & kLast) {
         // row sums of each query head: sum over the T rows of its KV head
@@ -712,7 +778,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         __syncwarp();
         if (lane == 0) mbar_arrive(l_bar);
         if (!warp_wait(l_bar, segs_done & 1, abort_flag)) { ok = false; break; }
-        if (!warp_wait(pv_done, j & 1, abort_flag)) { ok = false; break; }
+        if (!warp_wait(pv_done(j & 1), (j >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         // O^T lane r is output dim r: write every query head's value of this dim
         for (int c0 = 0; c0 < N; c0 += 16) {
@@ -805,9 +871,8 @@ TcgKernel tcg_kernel_for(int t, int g, bool f8) {
   }
 }
 
-// fp8 keeps two stages: the raw rings take the room of the third
 int pick_stages(int n_cols, bool f8) {
-  for (int s = f8 ? 2 : 3; s >= 2; --s)
+  for (int s = 3; s >= 2; --s)
     if (g_layout(s, n_cols, f8).total + 1024 <= 227 * 1024) return s;
   return 0;
 }
@@ -854,6 +919,10 @@ cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *
   if (!maps_ok) return cudaErrorInvalidValue;
   int tmem_cols = 32;
   while (tmem_cols < 3 * n_cols + 16) tmem_cols <<= 1;
+  if (f8) {  // O^T and S^T below column kK0, then the f16 K stages
+    if (3 * n_cols + 16 > static_cast<int>(kK0)) return cudaErrorInvalidValue;
+    tmem_cols = 512;
+  }
   GParams p;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.block_tables = a.block_tables;
