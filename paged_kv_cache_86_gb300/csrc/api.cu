@@ -271,10 +271,10 @@ size_t pkv_mixed_workspace_size(int32_t num_decode_seqs, int32_t num_q_heads,
       num_q_heads % num_kv_heads != 0)
     return 0;
   const size_t lens = (sizeof(int32_t) * (size_t(num_decode_seqs) + 1) + 255) & ~size_t(255);
-  if (num_decode_seqs == 0) return lens;
+  if (num_decode_seqs == 0) return lens + pkv::kPrefillWorkspace;
   cudaError_t e;
   const size_t dec = pkv::decode_workspace_upper_bound(num_decode_seqs, num_q_heads, num_kv_heads, &e);
-  return dec == 0 ? 0 : lens + dec;
+  return dec == 0 ? 0 : lens + dec + pkv::kPrefillWorkspace;
 }
 
 pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void *value,
@@ -296,6 +296,7 @@ pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void 
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_SHAPE;
   if (int64_t(max_seqlen_k) > int64_t(max_blocks_per_seq) * block_size) return PKV_ERR_ARG;
   if (total_q < num_decode_seqs || num_seqs - num_decode_seqs > 65535) return PKV_ERR_ARG;
+  if ((int64_t(max_seqlen_q) + 127) / 128 > 65535) return PKV_ERR_ARG;
   if (num_seqs == 0 || total_q == 0) return PKV_OK;
   if (!out || !q || !key || !value || !slot_mapping || !k_cache || !v_cache || !cu_seqlens_q ||
       !cu_seqlens_k || !block_tables || !workspace)
@@ -318,7 +319,8 @@ pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void 
   const size_t lens_bytes = (sizeof(int32_t) * (size_t(num_decode_seqs) + 1) + 255) & ~size_t(255);
   const size_t dec_bytes = num_decode_seqs > 0
       ? pkv::decode_workspace_bytes(num_decode_seqs, num_q_heads, num_kv_heads, plan) : 0;
-  if (workspace_bytes < lens_bytes + dec_bytes) return PKV_ERR_WORKSPACE;
+  const size_t dec_aligned = (dec_bytes + 255) & ~size_t(255);
+  if (workspace_bytes < lens_bytes + dec_aligned + pkv::kPrefillWorkspace) return PKV_ERR_WORKSPACE;
   uint32_t *err = pkv::device_error_word(&e);
   if (!err) return PKV_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -375,6 +377,7 @@ pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void 
     a.scale = scale;
     a.causal = 1;
     a.err = err;
+    a.workspace = static_cast<uint8_t *>(workspace) + lens_bytes + dec_aligned;
     if ((e = pkv::launch_paged_prefill(a, st)) != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
@@ -386,7 +389,7 @@ size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t num
   (void)total_q;
   (void)num_q_heads;
   (void)head_dim;
-  return 0;
+  return pkv::kPrefillWorkspace;
 }
 
 pkv_status pkv_paged_prefill(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -397,8 +400,6 @@ pkv_status pkv_paged_prefill(void *out, const void *q, const void *k_cache, cons
                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                              int32_t num_blocks, float scale, int32_t causal, void *workspace,
                              size_t workspace_bytes, pkv_dtype dtype, void *stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (dtype != PKV_BF16) return PKV_ERR_DTYPE;
   if (num_seqs < 0 || total_q < 0 || num_q_heads < 1 || num_kv_heads < 1 || block_size < 1 ||
       num_blocks < 1 || max_blocks_per_seq < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
@@ -408,9 +409,13 @@ pkv_status pkv_paged_prefill(void *out, const void *q, const void *k_cache, cons
   if (int64_t(max_seqlen_k) > int64_t(max_blocks_per_seq) * block_size) return PKV_ERR_ARG;
   if (!pkv::prefill_supported(num_q_heads, num_kv_heads, block_size)) return PKV_ERR_SHAPE;
   if (num_seqs > 65535 || num_q_heads > 65535) return PKV_ERR_ARG;  // grid y / z limits
+  if ((int64_t(max_seqlen_q) + 127) / 128 > 65535) return PKV_ERR_ARG;
   if (num_seqs == 0 || total_q == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_tables)
     return PKV_ERR_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < pkv::kPrefillWorkspace)
+    return PKV_ERR_WORKSPACE;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_ARG;
   cudaError_t e;
@@ -436,6 +441,7 @@ pkv_status pkv_paged_prefill(void *out, const void *q, const void *k_cache, cons
   a.scale = scale;
   a.causal = causal;
   a.err = err;
+  a.workspace = workspace;
   return from_cuda(pkv::launch_paged_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -123,7 +123,12 @@ struct PrefillArgs {
   float scale;
   int32_t causal;
   uint32_t *err;
+  // kPrefillWorkspace bytes of device scratch (the work ticket of the
+  // persistent kernel), 256-byte aligned
+  void *workspace = nullptr;
 };
+
+constexpr size_t kPrefillWorkspace = 256;
 
 bool prefill_supported(int num_q_heads, int num_kv_heads, int block_size);
 cudaError_t launch_paged_prefill(const PrefillArgs &a, cudaStream_t stream);

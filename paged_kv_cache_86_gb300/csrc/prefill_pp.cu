@@ -49,9 +49,9 @@ constexpr int kVStages = 2;
 constexpr int kThreads = 384;        // softmax A (warpgroup 0), softmax B (1), loaders + MMA (2)
 constexpr int kWarpQK = 8, kWarpMma = 9, kWarpV = 10;
 // Register split: launched at 168 per thread (384 x 168 = 64512); warpgroup 2
-// drops to 88 and the two softmax warpgroups rise to 208, which adds back up
-// to the launch total: 2 x 128 x 208 + 128 x 88 = 64512.
-constexpr int kRegsLaunch = 168, kRegsLow = 88, kRegsHigh = 208;
+// drops to 104 and the two softmax warpgroups rise to 200, which adds back up
+// to the launch total: 2 x 128 x 200 + 128 x 104 = 64512.
+constexpr int kRegsLaunch = 168, kRegsLow = 104, kRegsHigh = 200;
 static_assert(2 * 128 * kRegsHigh + 128 * kRegsLow == kThreads * kRegsLaunch,
               "setmaxnreg split must add up to the launch allocation");
 constexpr int kTmemCols = 512;
@@ -62,8 +62,11 @@ constexpr int kOffQ = 0;                              // Q_A, Q_B
 constexpr int kOffK = kOffQ + 2 * kTileBytes;
 constexpr int kOffV = kOffK + kKStages * kTileBytes;
 constexpr int kOffBar = kOffV + kVStages * kTileBytes;
-constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 6;  // q, k full/empty, v full/empty, s/p/pv x2
-constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+constexpr int kItemRing = 4;         // work items handed from the Q/K loader to the other roles
+// q, k/v full/empty, s/p/pv x2, q_empty, o_free x2, item full/empty x kItemRing
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 9 + 2 * kItemRing;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 4 * kItemRing + 1024;
+constexpr int kItemReaders = 1 + 1 + 8;   // V loader, MMA issuer, eight softmax warps
 
 struct PPParams {
   __nv_bfloat16 *out;
@@ -81,6 +84,8 @@ struct PPParams {
   int max_seqlen_k;
   int causal;
   int box_rows;
+  int q_tiles;       // 128-row query tiles of the longest chunk
+  uint32_t *ticket;  // next unclaimed work item (zeroed before the launch)
   float scale_log2;
   uint32_t *err;
 };
@@ -136,24 +141,38 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int seq = blockIdx.z;
-  const int qh_a = 2 * blockIdx.y;       // query heads qh_a, qh_a + 1 share KV head qh_a / G
-  const int r0 = blockIdx.x * kTile;
-
-  const int q_begin = p.cu_q[seq], q_end = p.cu_q[seq + 1];
-  const int k_len = p.cu_k[seq + 1] - p.cu_k[seq];
-  const int q_len = q_end - q_begin;
-  if (q_len < 0 || q_len > p.max_seqlen_q || q_end > p.total_q || k_len < 0 ||
-      k_len > p.max_seqlen_k || (p.causal && q_len > k_len)) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, PKV_DEVERR_LENGTH);
-    return;
-  }
-  if (r0 >= q_len) return;
-  const int prefix = p.causal ? k_len - q_len : 0;
-  const int last_row = min(r0 + kTile - 1, q_len - 1);
-  const int key_end = p.causal ? min(prefix + last_row + 1, k_len) : k_len;
-  const int n_tiles = (key_end + kTile - 1) / kTile;
-  const int kvh = qh_a / p.group;
+  // Persistent: each CTA claims work items from a global ticket (the Q/K loader
+  // takes the next one when it starts an item and passes it to the other roles
+  // through a small ring), so long and short items balance across SMs. Item w
+  // is query tile (last first) w % n_xt of head pair (w / n_xt) % n_hp of
+  // sequence w / (n_xt * n_hp): items claimed close in time read the K/V of a
+  // few sequences (L2 reuse). All roles walk the same items, skip the same ones.
+  const int n_xt = p.q_tiles, n_hp = p.num_q_heads / 2;
+  const int n_items = n_xt * n_hp * p.num_seqs;
+  struct Item {
+    int seq, qh_a, r0, q_begin, q_len, k_len, prefix, n_tiles, kvh;
+  };
+  auto item_at = [&](int w, Item &it) -> bool {
+    it.r0 = (n_xt - 1 - w % n_xt) * kTile;
+    it.qh_a = 2 * ((w / n_xt) % n_hp);
+    it.seq = w / (n_xt * n_hp);
+    it.q_begin = p.cu_q[it.seq];
+    const int q_end = p.cu_q[it.seq + 1];
+    it.k_len = p.cu_k[it.seq + 1] - p.cu_k[it.seq];
+    it.q_len = q_end - it.q_begin;
+    if (it.q_len < 0 || it.q_len > p.max_seqlen_q || q_end > p.total_q || it.k_len < 0 ||
+        it.k_len > p.max_seqlen_k || (p.causal && it.q_len > it.k_len)) {
+      if (threadIdx.x == 0 && it.qh_a == 0 && it.r0 == 0) raise_error(p.err, PKV_DEVERR_LENGTH);
+      return false;
+    }
+    if (it.r0 >= it.q_len) return false;
+    it.prefix = p.causal ? it.k_len - it.q_len : 0;
+    const int last_row = min(it.r0 + kTile - 1, it.q_len - 1);
+    const int key_end = p.causal ? min(it.prefix + last_row + 1, it.k_len) : it.k_len;
+    it.n_tiles = (key_end + kTile - 1) / kTile;
+    it.kvh = it.qh_a / p.group;
+    return true;
+  };
 
   const uint32_t bar0 = base + kOffBar;
   const uint32_t q_full = bar0;
@@ -165,11 +184,17 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   auto s_full = [&](int x) { return bar0 + 8u * (kB + x); };
   auto p_full = [&](int x) { return bar0 + 8u * (kB + 2 + x); };
   auto pv_done = [&](int x) { return bar0 + 8u * (kB + 4 + x); };
+  const uint32_t q_empty = bar0 + 8u * (kB + 6);                         // last S of an item done
+  auto o_free = [&](int x) { return bar0 + 8u * (kB + 7 + x); };         // O_X read out
+  auto item_full = [&](int i) { return bar0 + 8u * (kB + 9 + i); };
+  auto item_empty = [&](int i) { return bar0 + 8u * (kB + 9 + kItemRing + i); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + kNumBars * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *item_ring = reinterpret_cast<volatile int *>(smem + kOffBar + kNumBars * 8 + 16);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
@@ -182,6 +207,11 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(s_full(x), 1);
       mbar_init(p_full(x), 4);
       mbar_init(pv_done(x), 1);
+      mbar_init(o_free(x), 4);
+    }
+    for (int i = 0; i < kItemRing; ++i) {
+      mbar_init(item_full(i), 1);
+      mbar_init(item_empty(i), kItemReaders);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -203,6 +233,19 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     *abort_flag = 1;
     raise_error(p.err, PKV_DEVERR_TIMEOUT);
   };
+  // The n-th item of this CTA for a reader role (a whole warp, or lane 0 of the
+  // MMA warp alone): -1 on a timeout; n_items or more ends the walk.
+  auto read_item = [&](int n, bool whole_warp) -> int {
+    const int slot = n % kItemRing;
+    const uint32_t par = (n / kItemRing) & 1;
+    const bool got = whole_warp ? warp_wait(item_full(slot), par, abort_flag)
+                                : mbar_wait(item_full(slot), par, abort_flag);
+    if (!got) return -1;
+    const int w = item_ring[slot];
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || lane == 0) mbar_arrive(item_empty(slot));
+    return w;
+  };
 
   if (warp >= 8) {
     // The loader / MMA warpgroup hands registers to the softmax warpgroups;
@@ -211,36 +254,79 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegsLow));
     if (warp == kWarpQK || warp == kWarpV) {
       // ------------------------------------------------------------ producers
-      // one warp loads Q_A, Q_B and the K tiles, the other the V tiles
+      // one warp loads Q_A, Q_B and the K tiles, the other the V tiles; the
+      // rings run on across items, so the next item's loads overlap the end of
+      // the current one
       const bool is_k = warp == kWarpQK;
       const int stages = is_k ? kKStages : kVStages;
-      int issued = 0;
+      int issued = 0, items = 0;
       bool ok = true;
-      if (n_tiles > 0) {
-        if (lane == 0) {
-          if (is_k) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
-            for (int x = 0; x < 2; ++x) {
-              tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, qh_a + x, q_begin + r0, q_full);
-              tma_load_3d(sQ + x * kTileBytes + kRegion, &tm_q, 64, qh_a + x, q_begin + r0, q_full);
+      if (lane == 0) {
+        if (is_k) {
+          tma_prefetch_desc(&tm_q);
+          tma_prefetch_desc(&tm_k);
+        } else {
+          tma_prefetch_desc(&tm_v);
+        }
+      }
+      const int R = p.box_rows;
+      const int pieces = kTile / R;
+      const int oob_row = p.num_blocks * p.block_size;
+      Item it;
+      for (int n = 0; ok; ++n) {
+        int w;
+        if (is_k) {  // claim the next item and hand it to the readers
+          w = -1;
+          if (lane == 0) {
+            const int slot = n % kItemRing;
+            if (n >= kItemRing &&
+                !mbar_wait(item_empty(slot), ((n / kItemRing) - 1) & 1, abort_flag)) {
+              fail();
+            } else {
+              w = static_cast<int>(atomicAdd(p.ticket, 1u));
+              item_ring[slot] = w;
+              mbar_arrive(item_full(slot));
             }
-          } else {
-            tma_prefetch_desc(&tm_v);
+          }
+          w = __shfl_sync(0xffffffffu, w, 0);
+        } else {
+          w = read_item(n, true);
+        }
+        if (w < 0) {
+          ok = false;
+          break;
+        }
+        if (w >= n_items) break;
+        if (!item_at(w, it) || it.n_tiles == 0) continue;
+        if (is_k) {
+          int good = 1;
+          if (lane == 0) {
+            // Q_A, Q_B are reloaded once the previous item's last S MMA is done
+            if (items > 0 && !mbar_wait(q_empty, (items - 1) & 1, abort_flag)) {
+              good = 0;
+              fail();
+            } else {
+              mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+              for (int x = 0; x < 2; ++x) {
+                tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, it.qh_a + x, it.q_begin + it.r0, q_full);
+                tma_load_3d(sQ + x * kTileBytes + kRegion, &tm_q, 64, it.qh_a + x, it.q_begin + it.r0,
+                            q_full);
+              }
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, good, 0)) {
+            ok = false;
+            break;
           }
         }
-        const int R = p.box_rows;
-        const int pieces = kTile / R;
-        const int oob_row = p.num_blocks * p.block_size;
-        const int32_t *bt = p.block_tables + static_cast<size_t>(seq) * p.max_blocks_per_seq;
-        for (int j = 0; ok && j < n_tiles; ++j) {
-          const int s = j % stages;
-          const int round = j / stages;
+        const int32_t *bt = p.block_tables + static_cast<size_t>(it.seq) * p.max_blocks_per_seq;
+        for (int j = 0; ok && j < it.n_tiles; ++j) {
+          const int s = issued % stages;
+          const int round = issued / stages;
           int row = oob_row;
           if (lane < pieces) {
             const int key = j * kTile + lane * R;
-            if (key < k_len) {
+            if (key < it.k_len) {
               const int blk = __ldg(bt + key / p.block_size);
               if (blk >= 0 && blk < p.num_blocks) row = blk * p.block_size + key % p.block_size;
               else if (is_k) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
@@ -265,67 +351,91 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             break;
           }
           if (lane < pieces) {
-            tma_load_3d(dst + lane * R * 128, map, 0, kvh, row, full);
-            tma_load_3d(dst + kRegion + lane * R * 128, map, 64, kvh, row, full);
+            tma_load_3d(dst + lane * R * 128, map, 0, it.kvh, row, full);
+            tma_load_3d(dst + kRegion + lane * R * 128, map, 64, it.kvh, row, full);
           }
           ++issued;
         }
-        if (lane == 0) {  // drain: the last copies must land before the CTA exits
-          if (is_k) mbar_wait(q_full, 0, nullptr);
-          for (int j = max(0, issued - stages); j < issued; ++j)
-            mbar_wait(is_k ? k_full(j % stages) : v_full(j % stages), (j / stages) & 1, nullptr);
-        }
+        ++items;
+      }
+      if (lane == 0) {  // drain: the last copies must land before the CTA exits
+        if (is_k && items > 0) mbar_wait(q_full, (items - 1) & 1, nullptr);
+        for (int j = max(0, issued - stages); j < issued; ++j)
+          mbar_wait(is_k ? k_full(j % stages) : v_full(j % stages), (j / stages) & 1, nullptr);
       }
     } else if (warp == kWarpMma) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0 && n_tiles > 0) {
+      if (lane == 0) {
         constexpr uint32_t idesc_s = umma_idesc_bf16(kTile, kTile, false);
         constexpr uint32_t idesc_pv = umma_idesc_bf16(kTile, kHD, true);  // B (V) MN-major
-        bool ok = mbar_wait(q_full, 0, abort_flag);
+        bool ok = true;
         int s_commits[2] = {0, 0}, pv_commits[2] = {0, 0};
-        auto issue_s = [&](int x, int j) {
-          const int s = j % kKStages;
+        int kbase = 0, vbase = 0, items = 0;
+        auto issue_s = [&](int x, int kt, bool last_s) {
+          const int s = kt % kKStages;
           const uint32_t q = sQ + x * kTileBytes;
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < kHD / 16; ++kk)
             umma_bf16(tmem_s(x), desc_kmajor(q, kk), desc_kmajor(sK(s), kk), idesc_s, kk > 0 ? 1u : 0u);
           umma_commit(s_full(x));
           ++s_commits[x];
-          if (x == 1) umma_commit(k_empty(s));   // K(j) has fed both heads
+          if (x == 1) {
+            umma_commit(k_empty(s));             // K has fed both heads
+            if (last_s) umma_commit(q_empty);    // the item's Q_A, Q_B are no longer read
+          }
         };
-        auto issue_pv = [&](int x, int j) -> bool {
-          const int s = j % kVStages;
-          if (!mbar_wait(p_full(x), j & 1, abort_flag)) return false;
+        auto issue_pv = [&](int x, int j, int vt) -> bool {
+          const int s = vt % kVStages;
+          if (!mbar_wait(p_full(x), pv_commits[x] & 1, abort_flag)) return false;
+          // the first PV of an item overwrites O_X: the previous item's epilogue
+          // must have read it out
+          if (j == 0 && items > 0 && !mbar_wait(o_free(x), (items - 1) & 1, abort_flag)) return false;
           tc_fence_after();
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
             umma_bf16_tmem_a(tmem_o(x), tmem_s(x) + kk * 8, desc_v_mnmajor(sV(s), kk), idesc_pv,
                              (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(pv_done(x));
           ++pv_commits[x];
-          if (x == 1) umma_commit(v_empty(s));   // V(j) has fed both heads
+          if (x == 1) umma_commit(v_empty(s));   // V has fed both heads
           return true;
         };
-        // S_A(0), S_B(0), then per tile: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
-        if (ok) ok = mbar_wait(k_full(0), 0, abort_flag);
-        if (ok) {
+        Item it;
+        for (int n = 0; ok; ++n) {
+          const int w = read_item(n, false);
+          if (w < 0) {
+            ok = false;
+            break;
+          }
+          if (w >= n_items) break;
+          if (!item_at(w, it) || it.n_tiles == 0) continue;
+          const int nt = it.n_tiles;
+          // S_A(0), S_B(0), then per tile: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+          ok = mbar_wait(q_full, items & 1, abort_flag) &&
+               mbar_wait(k_full(kbase % kKStages), (kbase / kKStages) & 1, abort_flag);
+          if (!ok) break;
           tc_fence_after();
-          issue_s(0, 0);
-          issue_s(1, 0);
-        }
-        for (int j = 0; ok && j < n_tiles; ++j) {
-          const int sv = j % kVStages;
-          if (!mbar_wait(v_full(sv), (j / kVStages) & 1, abort_flag)) { ok = false; break; }
-          const bool more = j + 1 < n_tiles;
-          const int s1 = (j + 1) % kKStages;
-          for (int x = 0; ok && x < 2; ++x) {
-            if (!issue_pv(x, j)) { ok = false; break; }
-            if (more) {
-              if (x == 0 && !mbar_wait(k_full(s1), ((j + 1) / kKStages) & 1, abort_flag)) { ok = false; break; }
-              tc_fence_after();
-              issue_s(x, j + 1);
+          issue_s(0, kbase, false);
+          issue_s(1, kbase, nt == 1);
+          for (int j = 0; ok && j < nt; ++j) {
+            const int vt = vbase + j, kt1 = kbase + j + 1;
+            if (!mbar_wait(v_full(vt % kVStages), (vt / kVStages) & 1, abort_flag)) { ok = false; break; }
+            const bool more = j + 1 < nt;
+            for (int x = 0; ok && x < 2; ++x) {
+              if (!issue_pv(x, j, vt)) { ok = false; break; }
+              if (more) {
+                if (x == 0 && !mbar_wait(k_full(kt1 % kKStages), (kt1 / kKStages) & 1, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                issue_s(x, kt1, j + 2 == nt);
+              }
             }
           }
+          kbase += nt;
+          vbase += nt;
+          ++items;
         }
         if (!ok) fail();
         for (int x = 0; x < 2; ++x) {  // every issued MMA completes before TMEM is freed
@@ -342,111 +452,127 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int quad = warp & 3;                       // TMEM lanes 32*quad .. 32*quad+31
     const int r = quad * 32 + lane;                  // query row inside the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const int qpos = prefix + r0 + r;
-    const int visible = p.causal ? min(qpos + 1, k_len) : k_len;
     const float c = p.scale_log2;
-    float m_used = -INFINITY, l_sum = 0.f;           // running max of raw scores, row sum
     bool ok = true;
-
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      if (!warp_wait(s_full(x), j & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      float s[kTile];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        tmem_ld32(tmem_s(x) + lane_off + cc * 32, *reinterpret_cast<float(*)[32]>(s + cc * 32));
-      tmem_wait_ld();
-
-      const int key0 = j * kTile;
-      if (key0 + kTile > visible) {
-#pragma unroll
-        for (int e = 0; e < kTile; ++e) s[e] = (key0 + e < visible) ? s[e] : -INFINITY;
+    int tiles_done = 0;                              // S_X tiles consumed over all items
+    Item it;
+    for (int n = 0; ok; ++n) {
+      const int w = read_item(n, true);
+      if (w < 0) {
+        ok = false;
+        break;
       }
-      const float mt = max128(s);
-      // lazy rescale: only when the maximum grows by more than 2^8 after scaling
-      const bool grow = mt != -INFINITY && (m_used == -INFINITY || (mt - m_used) * c > kRescaleThreshold);
-      float alpha = 1.f;
-      if (grow) {
-        if (m_used != -INFINITY) {
-          alpha = ex2((m_used - mt) * c);
-          l_sum *= alpha;
+      if (w >= n_items) break;
+      if (!item_at(w, it)) continue;
+      const int qpos = it.prefix + it.r0 + r;
+      const int visible = p.causal ? min(qpos + 1, it.k_len) : it.k_len;
+      float m_used = -INFINITY, l_sum = 0.f;         // running max of raw scores, row sum
+
+      for (int j = 0; ok && j < it.n_tiles; ++j) {
+        if (!warp_wait(s_full(x), (tiles_done + j) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        float s[kTile];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          tmem_ld32(tmem_s(x) + lane_off + cc * 32, *reinterpret_cast<float(*)[32]>(s + cc * 32));
+        tmem_wait_ld();
+
+        const int key0 = j * kTile;
+        if (key0 + kTile > visible) {
+#pragma unroll
+          for (int e = 0; e < kTile; ++e) s[e] = (key0 + e < visible) ? s[e] : -INFINITY;
         }
-        m_used = mt;
-      }
-      // O_X holds PV_X(0..j-1), complete because S_X(j) completed after it; the
-      // TMEM loads and stores are warp-collective, so the whole warp takes part
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const float mt = max128(s);
+        // lazy rescale: only when the maximum grows by more than 2^8 after scaling
+        const bool grow = mt != -INFINITY && (m_used == -INFINITY || (mt - m_used) * c > kRescaleThreshold);
+        float alpha = 1.f;
+        if (grow) {
+          if (m_used != -INFINITY) {
+            alpha = ex2((m_used - mt) * c);
+            l_sum *= alpha;
+          }
+          m_used = mt;
+        }
+        // O_X holds PV_X(0..j-1), complete because S_X(j) completed after it; the
+        // TMEM loads and stores are warp-collective, so the whole warp takes part
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          float o[32];
+          for (int cc = 0; cc < 4; ++cc) {
+            float o[32];
+            tmem_ld32(tmem_o(x) + lane_off + cc * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(tmem_o(x) + lane_off + cc * 32, o);
+          }
+          tmem_wait_st();
+        }
+        // P = exp2(s*c - m*c) as bf16 pairs over TMEM columns 0..63 of S_X; the
+        // scaling and the row sum run two lanes per instruction (FFMA2 / FADD2).
+        const float mc = m_used * c;
+        float2 rs2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rs2[i] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float2 xx = ffma2(make_float2(s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]),
+                                    make_float2(c, c), make_float2(-mc, -mc));
+            const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+            rs2[e & 3] = fadd2(rs2[e & 3], pp);
+            pk[e] = float2_to_bf16x2(pp.x, pp.y);
+          }
+          tmem_st32_u(tmem_s(x) + lane_off + half * 32, pk);
+        }
+        const float2 rs01 = fadd2(rs2[0], rs2[1]), rs23 = fadd2(rs2[2], rs2[3]);
+        l_sum += (rs01.x + rs01.y) + (rs23.x + rs23.y);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(x));
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16 rows, then O_X is handed back for the next item
+      const bool have = it.n_tiles > 0;
+      if (have) {
+        ok = warp_wait(pv_done(x), (tiles_done + it.n_tiles - 1) & 1, abort_flag);
+        tc_fence_after();
+      }
+      const bool store = (it.r0 + r) < it.q_len;
+      __nv_bfloat16 *orow = p.out + (static_cast<size_t>(it.q_begin) + it.r0 + r) * p.num_q_heads * kHD +
+                            static_cast<size_t>(it.qh_a + x) * kHD;
+      const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float o[32];
+        if (have && ok) {
           tmem_ld32(tmem_o(x) + lane_off + cc * 32, o);
           tmem_wait_ld();
+        } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(tmem_o(x) + lane_off + cc * 32, o);
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
         }
-        tmem_wait_st();
-      }
-      // P = exp2(s*c - m*c) as bf16 pairs over TMEM columns 0..63 of S_X; the
-      // scaling and the row sum run two lanes per instruction (FFMA2 / FADD2).
-      const float mc = m_used * c;
-      float2 rs2[4];
+        if (store) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) rs2[i] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float2 xx = ffma2(make_float2(s[half * 64 + 2 * e], s[half * 64 + 2 * e + 1]),
-                                  make_float2(c, c), make_float2(-mc, -mc));
-          const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
-          rs2[e & 3] = fadd2(rs2[e & 3], pp);
-          pk[e] = float2_to_bf16x2(pp.x, pp.y);
-        }
-        tmem_st32_u(tmem_s(x) + lane_off + half * 32, pk);
-      }
-      const float2 rs01 = fadd2(rs2[0], rs2[1]), rs23 = fadd2(rs2[2], rs2[3]);
-      l_sum += (rs01.x + rs01.y) + (rs23.x + rs23.y);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(x));
-    }
-
-    if (!ok) fail();
-    // epilogue: O / l -> bf16 rows
-    const bool have = n_tiles > 0;
-    if (have && ok) {
-      ok = warp_wait(pv_done(x), (n_tiles - 1) & 1, abort_flag);
-      tc_fence_after();
-    }
-    const bool store = (r0 + r) < q_len;
-    __nv_bfloat16 *orow = p.out + (static_cast<size_t>(q_begin) + r0 + r) * p.num_q_heads * kHD +
-                          static_cast<size_t>(qh_a + x) * kHD;
-    const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
-#pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
-      float o[32];
-      if (have && ok) {
-        tmem_ld32(tmem_o(x) + lane_off + cc * 32, o);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0.f;
-      }
-      if (store) {
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + cc * 32);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 v;
-          v.x = float2_to_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
-          v.y = float2_to_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
-          v.z = float2_to_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
-          v.w = float2_to_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
-          dst[q4] = v;
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = float2_to_bf16x2(o[q4 * 8 + 0] * inv, o[q4 * 8 + 1] * inv);
+            v.y = float2_to_bf16x2(o[q4 * 8 + 2] * inv, o[q4 * 8 + 3] * inv);
+            v.z = float2_to_bf16x2(o[q4 * 8 + 4] * inv, o[q4 * 8 + 5] * inv);
+            v.w = float2_to_bf16x2(o[q4 * 8 + 6] * inv, o[q4 * 8 + 7] * inv);
+            dst[q4] = v;
+          }
         }
       }
+      if (have) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free(x));
+      }
+      tiles_done += it.n_tiles;
     }
     if (!ok) fail();
   }
@@ -532,7 +658,17 @@ cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
   p.box_rows = box_rows;
   p.scale_log2 = a.scale * kLog2e;
   p.err = a.err;
-  dim3 grid((a.max_seqlen_q + kTile - 1) / kTile, a.num_q_heads / 2, a.num_seqs);
+  p.q_tiles = (a.max_seqlen_q + kTile - 1) / kTile;
+  p.ticket = static_cast<uint32_t *>(a.workspace);
+  if (p.ticket == nullptr) return cudaErrorInvalidValue;
+  if (cudaError_t me = cudaMemsetAsync(p.ticket, 0, sizeof(uint32_t), stream)) return me;
+  const long long n_items = static_cast<long long>(p.q_tiles) * (a.num_q_heads / 2) * a.num_seqs;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
   prefill_pp_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
