@@ -329,11 +329,13 @@ pkv_status pkv_paged_decode_static_ws(void *out, const void *q,
  *   cu_seqlens_q/k    [num_seqs + 1] int32, non-decreasing, starting at 0;
  *                     q_len <= max_seqlen_q, k_len <= max_seqlen_k <=
  *                     max_blocks_per_seq * block_size, and q_len <= k_len when causal.
- *   workspace         at least pkv_prefill_workspace_size(...) bytes (0 today:
- *                     NULL is accepted).
- *   Supported: head_dim 128; num_q_heads / num_kv_heads in {1, 2, 4, 8};
- *   block_size a multiple of 16 or a power of two >= 1 ... see DESIGN notes in
- *   the implementation; unsupported shapes return PKV_ERR_SHAPE.
+ *   workspace         at least pkv_prefill_workspace_size(...) bytes (256),
+ *                     256-byte aligned: the work ticket of the persistent
+ *                     kernel, reset by the call itself; two calls in flight at
+ *                     once need two workspaces.
+ *   Supported: head_dim 128; num_q_heads a multiple of num_kv_heads;
+ *   block_size a multiple of 8; num_seqs and ceil(max_seqlen_q / 128) at most
+ *   65535. Unsupported shapes return PKV_ERR_SHAPE.
  */
 size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t total_q,
                                   int32_t num_q_heads, int32_t head_dim);
