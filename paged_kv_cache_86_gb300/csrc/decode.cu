@@ -120,6 +120,9 @@ decode_plan_kernel(const int32_t *__restrict__ context_lens, int num_seqs, int m
   __shared__ int base;
   int *cu = reinterpret_cast<int *>(ws + 256);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // the attention kernel is launched as a programmatic dependent of this one:
+  // it may start its prologue now and waits for this grid before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (blockIdx.x > 0) {
     // Decode step: one warp per sequence writes its newest token at logical
     // position n - 1, n = context_lens[i] clamped to [0, max_context_len] as
@@ -590,6 +593,8 @@ __device__ __forceinline__ long long combine_row(const CombineParams &p, int i, 
 constexpr int kCombineWarps = 8;
 
 __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const CombineParams p) {
+  // launched as a programmatic dependent of the attention kernel (a no-op otherwise)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   if (gw >= p.num_seqs * p.num_q_heads) return;
@@ -866,9 +871,23 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   const int warps = a.num_seqs * a.num_q_heads;
-  decode_combine_kernel<<<(warps + kCombineWarps - 1) / kCombineWarps, kCombineWarps * 32, 0,
-                          stream>>>(cp);
-  return cudaGetLastError();
+  const unsigned ctas = static_cast<unsigned>((warps + kCombineWarps - 1) / kCombineWarps);
+  if (plan.kind != 3) {
+    decode_combine_kernel<<<ctas, kCombineWarps * 32, 0, stream>>>(cp);
+    return cudaGetLastError();
+  }
+  // behind the all-heads tcgen05 kernel: a programmatic dependent launch hides
+  // the launch latency (the kernel waits for the attention grid first)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, cp);
 }
 
 }  // namespace pkv

@@ -263,11 +263,9 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int total = reinterpret_cast<const int *>(p.ws)[0];
-  const int range = reinterpret_cast<const int *>(p.ws)[1];
-  const int *cu = reinterpret_cast<const int *>(p.ws + 256);
-  const int lo = static_cast<int>(blockIdx.x) * range;
-  const int hi = min(lo + range, total);
+  // launched as a programmatic dependent of the plan kernel: let the combine
+  // pass behind this kernel be scheduled early too (it waits for this grid)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const uint32_t bar0 = base + L.bar;
   // K and V have their own rings: a K slot is free once S has been computed
@@ -336,6 +334,14 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything above overlapped the plan kernel; its outputs (ranges, prefix
+  // sums, the decode step's new tokens) are read only after this wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int total = reinterpret_cast<const int *>(p.ws)[0];
+  const int range = reinterpret_cast<const int *>(p.ws)[1];
+  const int *cu = reinterpret_cast<const int *>(p.ws + 256);
+  const int lo = static_cast<int>(blockIdx.x) * range;
+  const int hi = min(lo + range, total);
   const uint32_t tmem_o = tmem;                       // O^T: columns [0, N)
   auto tmem_s = [&](int b) { return tmem + N * (1 + b); };  // S^T buffers
   auto fail = [&]() {
@@ -948,8 +954,19 @@ cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *
   if (kern == nullptr) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, f8 ? kThreadsF8 : kThreads, smem, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the prologue (barriers, TMEM, descriptor
+  // prefetch) runs while the plan kernel finishes
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(f8 ? kThreadsF8 : kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
 }
 
 }  // namespace pkv
