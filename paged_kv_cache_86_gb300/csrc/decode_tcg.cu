@@ -62,6 +62,7 @@ constexpr int kMaxN = 128;
 constexpr int kMaxG = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.f;
+constexpr int kSoftmaxBarrier = 1;    // named barrier of the four softmax warps (0 is __syncthreads)
 
 enum : int { kFirst = 1, kLast = 2, kEnd = 4 };
 
@@ -281,7 +282,6 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // j only waits for PV(j-2) before writing, not for PV(j-1)
   auto p_full = [&](int b) { return bar0 + 8u * (b ? 33 : 12); };
   auto pv_done = [&](int b) { return bar0 + 8u * (b ? 32 : 13); };
-  const uint32_t x_bar = bar0 + 8u * 14;    // per-stage exchange among the softmax warps
   const uint32_t l_bar = bar0 + 8u * 15;    // per-segment row-sum exchange
   // fp8: the loaders' copies land on kr_full / vr_full; the converters then
   // fill the f16 stage and arrive on k_full / v_full
@@ -292,7 +292,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   GDesc *desc = reinterpret_cast<GDesc *>(smem + L.desc);
   float *alpha_buf = reinterpret_cast<float *>(smem + L.alpha);          // [2][kMaxN]
-  volatile int *grow_flag = reinterpret_cast<volatile int *>(alpha_buf + 2 * kMaxN);  // [2]
+  volatile int *stop_flag = reinterpret_cast<volatile int *>(alpha_buf + 2 * kMaxN);  // softmax warps leave
   float *lsum_buf = reinterpret_cast<float *>(smem + L.lsum);
   float *msum_buf = reinterpret_cast<float *>(smem + L.msum);
   const uint32_t sK = base + L.k, sV = base + L.v, sQ = base + L.q, sP = base + L.p;
@@ -300,7 +300,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // Q^T and P^T padding rows/columns must read as zeros for the whole kernel
   for (int i = threadIdx.x; i < (6 * static_cast<int>(small)) / 16; i += NT)
     reinterpret_cast<uint4 *>(smem + L.q)[i] = make_uint4(0u, 0u, 0u, 0u);
-  if (threadIdx.x < 2) grow_flag[threadIdx.x] = 0;
+  if (threadIdx.x == 0) *stop_flag = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(k_full(s), F8 ? 4 : 1);
@@ -320,7 +320,6 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(p_full(b), 4);
       mbar_init(pv_done(b), 1);
     }
-    mbar_init(x_bar, 4);
     mbar_init(l_bar, 4);
     *abort_flag = 0;
     fence_barrier_init();
@@ -489,15 +488,17 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       // V), so each is issued as soon as its own inputs are ready: S(j) when K(j)
       // has landed and S^T[j & 1] is free, PV(t) when P(t) and V(t) are ready.
       // The issuer polls both without blocking on either.
-      uint8_t first_of[8];        // kFirst of stage t, kept from S(t) until PV(t)
+      uint32_t first_of = 0;      // bit t & 31: kFirst of stage t, kept from S(t) until PV(t)
       int end_at = -1;            // index of the stage that ends the walk
-      unsigned long long idle_since = global_timer_ns();
+      unsigned long long idle_since = 0;
       for (uint32_t idle = 0;;) {
         bool did = false;
         if (end_at < 0 && s_issued - pv_issued < 4) {
           const int j = s_issued, s = j % S, buf = j & 1;
-          if (mbar_test_wait(k_full(s), (j / S) & 1) &&
-              (j < 2 || mbar_test_wait(s_free(buf), ((j - 2) >> 1) & 1))) {
+          // both probes are issued before either result is used
+          const bool k_ready = mbar_test_wait(k_full(s), (j / S) & 1);
+          const bool s_ready = j < 2 || mbar_test_wait(s_free(buf), ((j - 2) >> 1) & 1);
+          if (k_ready && s_ready) {
             const GDesc d = desc[s];
             if (d.flags & kEnd) {
               end_at = j;
@@ -515,7 +516,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               }
               umma_commit(s_full(buf));
               umma_commit(k_empty(s));
-              first_of[j & 7] = (d.flags & kFirst) ? 1 : 0;
+              first_of = (first_of & ~(1u << (j & 31))) | ((d.flags & kFirst) ? 1u << (j & 31) : 0u);
               ++s_issued;
             }
             did = true;
@@ -523,9 +524,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         if (pv_issued < s_issued) {
           const int t = pv_issued, s = t % S;
-          if (mbar_test_wait(v_full(s), (t / S) & 1) && mbar_test_wait(p_full(t & 1), (t >> 1) & 1)) {
+          const bool v_ready = mbar_test_wait(v_full(s), (t / S) & 1);
+          const bool p_ready = mbar_test_wait(p_full(t & 1), (t >> 1) & 1);
+          if (v_ready && p_ready) {
             tc_fence_after();
-            const bool first = first_of[t & 7] != 0;
+            const bool first = (first_of >> (t & 31)) & 1u;
 #pragma unroll
             for (int kk = 0; kk < kRows / 16; ++kk)
               umma_bf16(tmem_o, desc_v(sV + s * kKVBytes, kk), desc_k(sP + (t & 1) * 2 * small, kk, small),
@@ -537,11 +540,14 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           }
         }
         if (end_at >= 0 && pv_issued == s_issued) break;
+        // the clock is only read while idle: from the 256th empty poll on
         if (did) {
           idle = 0;
-          idle_since = global_timer_ns();
         } else if ((++idle & 255u) == 0) {
-          if (*abort_flag || global_timer_ns() - idle_since > kWaitTimeoutNs) {
+          const unsigned long long now = global_timer_ns();
+          if (idle == 256u) {
+            idle_since = now;
+          } else if (*abort_flag || now - idle_since > kWaitTimeoutNs) {
             ok = false;
             break;
           }
@@ -635,80 +641,149 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // P^T (N rows x 128 stage rows, K-major, 128-byte swizzle): element (n, r)
     const uint32_t p_half = (r >> 6) * small;
     const int rc = r & 63;
+    // The four softmax warps meet once per stage on a hardware barrier that
+    // also ORs a flag over their threads. The flag is raised when the maximum
+    // of a query head grew past the rescale threshold (rare: all four warps
+    // then rescale O^T together) or when a warp gave up on a wait (all four
+    // then leave the loop in the same stage, so none is left at the barrier).
+    // Between those events the warps exchange nothing: the common stage has
+    // no shared-memory round trip for the maximum and no shuffles.
     for (int j = 0;; ++j) {
       const int s = j % S;
-      if (!warp_wait(k_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
-      const GDesc d = desc[s];
-      // fp8: this row's K scale sits in the raw stage, which the loader may
-      // refill once every softmax warp has arrived on k_empty
-      float kscale = 1.f;
-      if (F8 && !(d.flags & kEnd))
-        kscale = reinterpret_cast<const float *>(smem + L.kr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(k_empty(s));  // this stage's descriptor has been read
-      if (d.flags & kEnd) break;
       const int buf = j & 1;
+      GDesc d = {0, 0, 0, 0, kEnd, 0, 0, 0};
+      float kscale = 1.f;
+      if (ok && !warp_wait(k_full(s), (j / S) & 1, abort_flag)) ok = false;
+      if (ok) {
+        d = desc[s];
+        // fp8: this row's K scale sits in the raw stage, which the loader may
+        // refill once every softmax warp has arrived on k_empty
+        if (F8 && !(d.flags & kEnd))
+          kscale = reinterpret_cast<const float *>(smem + L.kr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(k_empty(s));  // this stage's descriptor has been read
+      }
+      const bool end = ok && (d.flags & kEnd);
+      const bool work = ok && !end;
       const bool first = (d.flags & kFirst) != 0;
-      if (!warp_wait(s_full(buf), (j >> 1) & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      // the S^T columns of all heads of this warp in one load; keep this row's G
-      float cols[kCols];
-      tmem_ld_cols<kCols>(tmem_s(buf) + lane_off + warp_head0 * G, cols);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(buf));
-      float sc[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float v = cols[g];
-#pragma unroll
-        for (int k = 1; k < kHeadsInWarp; ++k) v = (my_slot == k) ? cols[k * G + g] : v;
-        sc[g] = v;
-      }
-
       const int tok = d.pa + t;
-      const bool valid = tok >= d.p0 && tok < d.p1;
-      float vmax[G];
+      const bool valid = work && tok >= d.p0 && tok < d.p1;
+      const bool partial = d.pa < d.p0 || d.pa + T > d.p1;
+      float sc[G];
+      bool need = false;
+      if (work && !warp_wait(s_full(buf), (j >> 1) & 1, abort_flag)) ok = false;
+      if (ok && work) {
+        tc_fence_after();
+        // the S^T columns of all heads of this warp in one load; keep this row's G
+        float cols[kCols];
+        tmem_ld_cols<kCols>(tmem_s(buf) + lane_off + warp_head0 * G, cols);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free(buf));
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        sc[g] = valid ? sc[g] * (F8 ? p.scale_log2 * kscale : p.scale_log2) : -INFINITY;
-        vmax[g] = sc[g];
-      }
-      // stage maximum of each query head over the T rows of its KV head (one warp)
+        for (int g = 0; g < G; ++g) {
+          float v = cols[g];
 #pragma unroll
-      for (int off = T >> 1; off >= 1; off >>= 1)
-#pragma unroll
-        for (int g = 0; g < G; ++g) vmax[g] = fmaxf(vmax[g], __shfl_xor_sync(0xffffffffu, vmax[g], off));
-      float alpha[G];
-      bool grow = false;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        alpha[g] = 1.f;
+          for (int k = 1; k < kHeadsInWarp; ++k) v = (my_slot == k) ? cols[k * G + g] : v;
+          sc[g] = valid ? v * (F8 ? p.scale_log2 * kscale : p.scale_log2) : -INFINITY;
+        }
         if (first) {
-          m_used[g] = vmax[g];
-        } else if (vmax[g] > m_used[g] + kRescaleThreshold) {
-          alpha[g] = ex2(m_used[g] - vmax[g]);
-          m_used[g] = vmax[g];
-          grow = true;
+          // a segment's first stage fixes the reference maximum of each query
+          // head: the maximum over the T rows of its KV head (one warp)
+          float vmax[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) vmax[g] = sc[g];
+#pragma unroll
+          for (int off = T >> 1; off >= 1; off >>= 1)
+#pragma unroll
+            for (int g = 0; g < G; ++g) vmax[g] = fmaxf(vmax[g], __shfl_xor_sync(0xffffffffu, vmax[g], off));
+#pragma unroll
+          for (int g = 0; g < G; ++g) m_used[g] = vmax[g];
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; ++g) need |= sc[g] > m_used[g] + kRescaleThreshold;
         }
       }
+      // PV(j-2) read this stage's P^T buffer: it must be done before the rewrite
+      if (ok && work && j >= 2) {
+        if (warp_wait(pv_done(buf), ((j - 2) >> 1) & 1, abort_flag)) tc_fence_after();
+        else ok = false;
+      }
+      // fp8: P^T rows carry the V row scale, read from the raw V stage as soon
+      // as it has landed; a partial stage zeroes its masked rows of the
+      // converted V stage, so it waits for the conversion
+      if (ok && work && (F8 || partial) &&
+          !warp_wait((F8 && !partial) ? vr_full(s) : v_full(s), (j / S) & 1, abort_flag))
+        ok = false;
+      if (!ok && lane == 0) {
+        *stop_flag = 1;
+        *abort_flag = 1;  // the other roles give up their waits too
+      }
+      if (bar_red_or(kSoftmaxBarrier, 128, need || !ok)) {
+        if (*stop_flag) {
+          ok = false;
+          break;
+        }
+        // some head's maximum grew (the flag is only raised in working stages,
+        // so every warp is in one): new maxima of every head, O^T rescaled
+        float vmax[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) vmax[g] = sc[g];
+#pragma unroll
+        for (int off = T >> 1; off >= 1; off >>= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) vmax[g] = fmaxf(vmax[g], __shfl_xor_sync(0xffffffffu, vmax[g], off));
+        float alpha[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          alpha[g] = 1.f;
+          if (vmax[g] > m_used[g] + kRescaleThreshold) {
+            alpha[g] = ex2(m_used[g] - vmax[g]);
+            m_used[g] = vmax[g];
+          }
+          l_part[g] *= alpha[g];
+        }
+        if (t == 0) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) alpha_buf[head * G + g] = alpha[g];
+        }
+        bar_sync(kSoftmaxBarrier, 128);
+        // O^T may only be rescaled once every earlier PV has landed in it
+        if (j >= 1) {
+          if (warp_wait(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag)) tc_fence_after();
+          else ok = false;
+        }
+        if (ok) {
+          for (int c0 = 0; c0 < N; c0 += 16) {
+            float o[16];
+            tmem_ld16(tmem_o + lane_off + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (c0 + e < p.num_q_heads) o[e] *= alpha_buf[c0 + e];
+            asm volatile(
+                "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+                :: "r"(tmem_o + lane_off + c0), "f"(o[0]), "f"(o[1]), "f"(o[2]), "f"(o[3]),
+                   "f"(o[4]), "f"(o[5]), "f"(o[6]), "f"(o[7]), "f"(o[8]), "f"(o[9]), "f"(o[10]),
+                   "f"(o[11]), "f"(o[12]), "f"(o[13]), "f"(o[14]), "f"(o[15])
+                : "memory");
+          }
+          tmem_wait_st();
+        }
+      }
+      if (end) break;
+      if (!ok) continue;  // the next stage's barrier takes every warp out
+
       // P^T values and running row sums
       float pr[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         pr[g] = valid ? ex2(sc[g] - m_used[g]) : 0.f;
-        l_part[g] = first ? pr[g] : l_part[g] * alpha[g] + pr[g];
+        l_part[g] = first ? pr[g] : l_part[g] + pr[g];
       }
-      // PV(j-2) read this stage's P^T buffer: it must be done before the rewrite
-      if (j >= 2) {
-        if (!warp_wait(pv_done(j & 1), ((j - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-      }
-      const uint32_t p_region = sP + (j & 1) * 2 * small + p_half;
-      const bool partial = d.pa < d.p0 || d.pa + T > d.p1;
-      // fp8: P^T rows carry the V row scale, read from the raw V stage
-      if ((F8 || partial) && !warp_wait(v_full(s), (j / S) & 1, abort_flag)) { ok = false; break; }
+      const uint32_t p_region = sP + buf * 2 * small + p_half;
       float vscale = 1.f;
       if (F8) vscale = reinterpret_cast<const float *>(smem + L.vr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
 #pragma unroll
@@ -727,43 +802,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" :: "r"(vrow + kRegion + c * 16), "r"(0u) : "memory");
         }
       }
-      // broadcast the rare O^T rescale of the heads whose maximum grew
-      float *abuf = alpha_buf + (j & 1) * kMaxN;
-      if (t == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) abuf[head * G + g] = alpha[g];
-        if (grow) grow_flag[j & 1] = j + 1;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(x_bar);
-      if (!warp_wait(x_bar, j & 1, abort_flag)) { ok = false; break; }
-      if (grow_flag[j & 1] == j + 1) {
-        // O^T may only be rescaled once every earlier PV has landed in it
-        if (j >= 1) {
-          if (!warp_wait(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-        }
-        for (int c0 = 0; c0 < N; c0 += 16) {
-          float o[16];
-          tmem_ld16(tmem_o + lane_off + c0, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            if (c0 + e < p.num_q_heads) o[e] *= abuf[c0 + e];
-          asm volatile(
-              "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-              "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
-              :: "r"(tmem_o + lane_off + c0), "f"(o[0]), "f"(o[1]), "f"(o[2]), "f"(o[3]),
-                 "f"(o[4]), "f"(o[5]), "f"(o[6]), "f"(o[7]), "f"(o[8]), "f"(o[9]), "f"(o[10]),
-                 "f"(o[11]), "f"(o[12]), "f"(o[13]), "f"(o[14]), "f"(o[15])
-              : "memory");
-        }
-        tmem_wait_st();
-      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(j & 1));
+      if (lane == 0) mbar_arrive(p_full(buf));
 
       if (d.flags & kLast) {
         // row sums of each query head: sum over the T rows of its KV head
@@ -783,8 +825,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(l_bar);
-        if (!warp_wait(l_bar, segs_done & 1, abort_flag)) { ok = false; break; }
-        if (!warp_wait(pv_done(j & 1), (j >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!warp_wait(l_bar, segs_done & 1, abort_flag) ||
+            !warp_wait(pv_done(buf), (j >> 1) & 1, abort_flag)) {
+          ok = false;
+          continue;
+        }
         tc_fence_after();
         // O^T lane r is output dim r: write every query head's value of this dim
         for (int c0 = 0; c0 < N; c0 += 16) {

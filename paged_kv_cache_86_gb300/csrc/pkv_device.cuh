@@ -158,6 +158,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// ------------------------------------------------------ named barriers --
+
+// Hardware barrier `id` over `nthreads` threads (whole warps) that also ORs
+// `v` over them; every participating warp must reach it the same number of
+// times. Orders the participants' shared-memory accesses like __syncthreads.
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r) : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads) : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void bar_sync(int id, int nthreads) {
+  asm volatile("barrier.cta.sync.aligned %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
 // ------------------------------------------------------------ bulk copy --
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

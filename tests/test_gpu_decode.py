@@ -190,3 +190,38 @@ def test_decode_rejects_shapes_no_kernel_covers():
         pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], m["block_tables"], m["context_lens"],
                          w.scale)
     assert e.value.status == -2
+
+
+def aligned_key(q_row, logit):
+    """A key whose scaled dot product with q_row (scale 1/sqrt(D)) is `logit`."""
+    q = q_row.float()
+    d = q.shape[0]
+    return (q * (logit * d ** 0.5 / float((q * q).sum()))).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("hkv,group", [(8, 4), (4, 8), (16, 2)])
+def test_decode_late_maximum_rescales_the_accumulator(hkv, group):
+    # keys aligned with one query head far into the context: a later stage's
+    # logit exceeds the reference maximum of the segment's first stage by much
+    # more than the lazy-rescale threshold, in heads handled by different
+    # softmax warps, twice in one sequence, and once at the new token itself
+    lens = [300, 2000, 700, 64, 4000, 17]
+    w = W.decode_workload(f"late_max_{hkv}x{group}", lens, hkv * group, hkv, 16, seed=321 + hkv)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    bs = w.block_size
+    # (logit 100 puts exp2 of the gap beyond bf16's range: without the rescale
+    # the P^T values would overflow)
+    spikes = [(0, 0.7, 30.0), (hkv // 2 - 1, 0.5, 12.0), (hkv - 3, 0.9, 9.0), (hkv - 3, 0.95, 40.0),
+              (hkv - 1, 0.3, 15.0), (1, 0.6, 100.0)]
+    for i, n in enumerate(lens):
+        for h, frac, logit in spikes:
+            pos = int(frac * (n - 1))           # an already cached position (< n - 1)
+            blk, off = int(w.block_tables[i, pos // bs]), pos % bs
+            g = (i + h) % group
+            t["k_cache"][blk, off, h] = aligned_key(t["q"][i, h * group + g], logit)
+        # the new token of this step is a spike too (quantized and stored first)
+        t["key"][i, hkv - 2] = aligned_key(t["q"][i, (hkv - 2) * group], 25.0)
+    ids = np.arange(w.num_seqs)
+    ref = decode_step_reference(w, ids, t["k_cache"], t["v_cache"], t["q"], t["key"], t["value"])
+    out = run_decode_step(w, t)
+    assert_close(out, ref, w.name)

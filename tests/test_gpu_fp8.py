@@ -99,3 +99,22 @@ def test_fp8_decode_rejects_shapes_without_the_kernel():
         pkv.paged_decode_fp8(t["q"], kc, vc, ks, vs, torch.from_numpy(w.block_tables).cuda(),
                              torch.from_numpy(w.context_lens).cuda(), w.scale)
     assert e.value.status == -2
+
+
+def test_fp8_decode_late_maximum_rescales_the_accumulator():
+    # the new token of each sequence is a key aligned with one query head: its
+    # logit exceeds the reference maximum of the segment's first stage by far
+    # more than the lazy-rescale threshold, in the last stage of the context
+    hkv, group, bs = 8, 4, 16
+    lens = [300, 2000, 700, 64, 17]
+    w = W.decode_workload("fp8_late_max", lens, hkv * group, hkv, bs, seed=4321)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    for i in range(len(lens)):
+        for h, logit in ((0, 30.0), (3, 12.0), (5, 9.0), (7, 20.0)):
+            q = t["q"][i, h * group + (i % group)].float()
+            t["key"][i, h] = (q * (logit * 128 ** 0.5 / float((q * q).sum()))).to(torch.bfloat16)
+    kc, vc, ks, vs = fp8_case(w, w.seed)
+    ids = np.arange(w.num_seqs)
+    ref, _ = oracle_step_fp8(w, ids, kc, vc, ks, vs, t)
+    out = step_fp8(w, t, kc, vc, ks, vs)
+    assert_close(out, ref, w.name)
