@@ -499,12 +499,12 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const bool k_ready = mbar_test_wait(k_full(s), (j / S) & 1);
           const bool s_ready = j < 2 || mbar_test_wait(s_free(buf), ((j - 2) >> 1) & 1);
           if (k_ready && s_ready) {
-            const GDesc d = desc[s];
-            if (d.flags & kEnd) {
+            const int flags = desc[s].flags;  // the only field the issuer needs
+            if (flags & kEnd) {
               end_at = j;
             } else {
               tc_fence_after();
-              const uint32_t q = sQ + d.qbuf * 2 * small;
+              const uint32_t q = sQ;  // one Q^T buffer
 #pragma unroll
               for (int kk = 0; kk < kHD / 16; ++kk) {
                 if (F8)
@@ -516,7 +516,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               }
               umma_commit(s_full(buf));
               umma_commit(k_empty(s));
-              first_of = (first_of & ~(1u << (j & 31))) | ((d.flags & kFirst) ? 1u << (j & 31) : 0u);
+              first_of = (first_of & ~(1u << (j & 31))) | ((flags & kFirst) ? 1u << (j & 31) : 0u);
               ++s_issued;
             }
             did = true;
@@ -716,6 +716,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (ok && work && (F8 || partial) &&
           !warp_wait((F8 && !partial) ? vr_full(s) : v_full(s), (j / S) & 1, abort_flag))
         ok = false;
+      // issued here so that the load overlaps the barrier below
+      float vscale = 1.f;
+      if (F8 && ok && work)
+        vscale = reinterpret_cast<const float *>(smem + L.vr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
       if (!ok && lane == 0) {
         *stop_flag = 1;
         *abort_flag = 1;  // the other roles give up their waits too
@@ -784,8 +788,6 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         l_part[g] = first ? pr[g] : l_part[g] + pr[g];
       }
       const uint32_t p_region = sP + buf * 2 * small + p_half;
-      float vscale = 1.f;
-      if (F8) vscale = reinterpret_cast<const float *>(smem + L.vr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const int n = head * G + g;
