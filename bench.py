@@ -351,23 +351,32 @@ def run_pkv(args, rank, world, device):
 
 
     # end to end through the public API with host buffers: H2D of the step's
-    # inputs from pinned memory, the decode step, D2H of the output
-    host = {"q": t["q"].cpu().pin_memory(), "key": kn.cpu().pin_memory(),
-            "value": vn.cpu().pin_memory()}
-    host_meta = {"bt": bt.cpu().pin_memory(), "cl": cl.cpu().pin_memory()}
+    # inputs from pinned memory, the decode step, D2H of the output. The inputs
+    # travel as one packed buffer (q, new K, new V, block tables, lengths at
+    # 256-byte aligned offsets) so a step makes one copy each way.
+    parts = [("q", t["q"]), ("key", kn), ("value", vn), ("bt", bt), ("cl", cl)]
+    offs, off = {}, 0
+    for k, v in parts:
+        offs[k] = off
+        off += (v.numel() * v.element_size() + 255) // 256 * 256
+    host_pack = torch.empty(off, dtype=torch.uint8).pin_memory()
+    dev_pack = torch.empty(off, dtype=torch.uint8, device=device)
+
+    def view(buf, k, like):
+        n = like.numel() * like.element_size()
+        return buf[offs[k]:offs[k] + n].view(like.dtype).view(like.shape)
+
+    for k, v in parts:
+        view(host_pack, k, v).copy_(v.cpu())
+    dev = {k: view(dev_pack, k, v) for k, v in parts}
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dev_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
-    dev_meta = {k: torch.empty_like(v, device=device) for k, v in host_meta.items()}
-    h2d = sum(v.numel() * v.element_size() for v in list(host.values()) + list(host_meta.values()))
+    h2d = sum(v.numel() * v.element_size() for _, v in parts)
     d2h = host_out.numel() * host_out.element_size()
 
     def e2e_step():
-        for k in host:
-            dev_in[k].copy_(host[k], non_blocking=True)
-        for k in host_meta:
-            dev_meta[k].copy_(host_meta[k], non_blocking=True)
-        pkv.decode_step(dev_in["q"], dev_in["key"], dev_in["value"], t["k_cache"], t["v_cache"],
-                        dev_meta["bt"], dev_meta["cl"], w.scale, out=out, workspace=ws)
+        dev_pack.copy_(host_pack, non_blocking=True)
+        pkv.decode_step(dev["q"], dev["key"], dev["value"], t["k_cache"], t["v_cache"],
+                        dev["bt"], dev["cl"], w.scale, out=out, workspace=ws)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):
