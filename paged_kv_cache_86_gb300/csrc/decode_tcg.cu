@@ -269,9 +269,9 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const uint32_t bar0 = base + L.bar;
-  // K and V have their own rings: a K slot is free once S has been computed
-  // from it and the softmax warps have read its stage descriptor; a V slot once
-  // the PV MMA that reads it has completed
+  // K and V have their own rings: a K slot is free once every softmax warp has
+  // seen S computed from it (which also means its stage descriptor was read);
+  // a V slot once the PV MMA that reads it has completed
   auto k_full = [&](int s) { return bar0 + 8u * s; };
   auto k_empty = [&](int s) { return bar0 + 8u * (4 + s); };
   auto v_full = [&](int s) { return bar0 + 8u * (16 + s); };
@@ -304,7 +304,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(k_full(s), F8 ? 4 : 1);
-      mbar_init(k_empty(s), 1 + 4);
+      mbar_init(k_empty(s), 4);
       mbar_init(v_full(s), F8 ? 4 : 1);
       mbar_init(v_empty(s), 1);
       if (F8) {
@@ -515,7 +515,6 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             idesc_s, kk > 0 ? 1u : 0u);
               }
               umma_commit(s_full(buf));
-              umma_commit(k_empty(s));
               first_of = (first_of & ~(1u << (j & 31))) | ((flags & kFirst) ? 1u << (j & 31) : 0u);
               ++s_issued;
             }
@@ -657,11 +656,9 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (ok) {
         d = desc[s];
         // fp8: this row's K scale sits in the raw stage, which the loader may
-        // refill once every softmax warp has arrived on k_empty
+        // refill once every softmax warp has arrived on k_empty (below)
         if (F8 && !(d.flags & kEnd))
           kscale = reinterpret_cast<const float *>(smem + L.kr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(k_empty(s));  // this stage's descriptor has been read
       }
       const bool end = ok && (d.flags & kEnd);
       const bool work = ok && !end;
@@ -680,7 +677,12 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(s_free(buf));
+        if (lane == 0) {
+          mbar_arrive(s_free(buf));
+          // S(j) has completed, so K(j) is no longer read; the descriptor and
+          // the K scales of this stage have been read too: the K slot is free
+          mbar_arrive(k_empty(s));
+        }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           float v = cols[g];
