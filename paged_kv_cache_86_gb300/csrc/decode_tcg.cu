@@ -493,50 +493,60 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       unsigned long long idle_since = 0;
       for (uint32_t idle = 0;;) {
         bool did = false;
+        // Probes first, MMAs after: a shared-memory access (a barrier probe, a
+        // descriptor load) that this thread issues behind its own MMAs waits
+        // until the tensor core has taken them, so each round reads everything
+        // it needs before it issues anything.
+        const int j = s_issued, sj = j % S, bj = j & 1;
+        const int t = pv_issued, st = t % S;
+        bool do_s = false, do_pv = false;
+        int flags = 0;
         if (end_at < 0 && s_issued - pv_issued < 4) {
-          const int j = s_issued, s = j % S, buf = j & 1;
-          // both probes are issued before either result is used
-          const bool k_ready = mbar_test_wait(k_full(s), (j / S) & 1);
-          const bool s_ready = j < 2 || mbar_test_wait(s_free(buf), ((j - 2) >> 1) & 1);
+          const bool k_ready = mbar_test_wait(k_full(sj), (j / S) & 1);
+          const bool s_ready = j < 2 || mbar_test_wait(s_free(bj), ((j - 2) >> 1) & 1);
           if (k_ready && s_ready) {
-            const int flags = desc[s].flags;  // the only field the issuer needs
+            flags = desc[sj].flags;  // the only field the issuer needs
             if (flags & kEnd) {
               end_at = j;
+              did = true;
             } else {
-              tc_fence_after();
-              const uint32_t q = sQ;  // one Q^T buffer
-#pragma unroll
-              for (int kk = 0; kk < kHD / 16; ++kk) {
-                if (F8)
-                  umma_tmem_a(tmem_s(buf), tmem + kK0 + s * 64 + kk * 8, desc_k(q, kk, small), idesc_s,
-                              kk > 0 ? 1u : 0u);
-                else
-                  umma_bf16(tmem_s(buf), desc_k(sK + s * kKVBytes, kk, kRegion), desc_k(q, kk, small),
-                            idesc_s, kk > 0 ? 1u : 0u);
-              }
-              umma_commit(s_full(buf));
-              first_of = (first_of & ~(1u << (j & 31))) | ((flags & kFirst) ? 1u << (j & 31) : 0u);
-              ++s_issued;
+              do_s = true;
             }
-            did = true;
           }
         }
         if (pv_issued < s_issued) {
-          const int t = pv_issued, s = t % S;
-          const bool v_ready = mbar_test_wait(v_full(s), (t / S) & 1);
+          const bool v_ready = mbar_test_wait(v_full(st), (t / S) & 1);
           const bool p_ready = mbar_test_wait(p_full(t & 1), (t >> 1) & 1);
-          if (v_ready && p_ready) {
-            tc_fence_after();
-            const bool first = (first_of >> (t & 31)) & 1u;
+          do_pv = v_ready && p_ready;
+        }
+        if (do_s) {
+          tc_fence_after();
+          const uint32_t q = sQ;  // one Q^T buffer
 #pragma unroll
-            for (int kk = 0; kk < kRows / 16; ++kk)
-              umma_bf16(tmem_o, desc_v(sV + s * kKVBytes, kk), desc_k(sP + (t & 1) * 2 * small, kk, small),
-                        idesc_pv, (first && kk == 0) ? 0u : 1u);
-            umma_commit(pv_done(t & 1));
-            umma_commit(v_empty(s));
-            ++pv_issued;
-            did = true;
+          for (int kk = 0; kk < kHD / 16; ++kk) {
+            if (F8)
+              umma_tmem_a(tmem_s(bj), tmem + kK0 + sj * 64 + kk * 8, desc_k(q, kk, small), idesc_s,
+                          kk > 0 ? 1u : 0u);
+            else
+              umma_bf16(tmem_s(bj), desc_k(sK + sj * kKVBytes, kk, kRegion), desc_k(q, kk, small),
+                        idesc_s, kk > 0 ? 1u : 0u);
           }
+          umma_commit(s_full(bj));
+          first_of = (first_of & ~(1u << (j & 31))) | ((flags & kFirst) ? 1u << (j & 31) : 0u);
+          ++s_issued;
+          did = true;
+        }
+        if (do_pv) {
+          tc_fence_after();
+          const bool first = (first_of >> (t & 31)) & 1u;
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk)
+            umma_bf16(tmem_o, desc_v(sV + st * kKVBytes, kk), desc_k(sP + (t & 1) * 2 * small, kk, small),
+                      idesc_pv, (first && kk == 0) ? 0u : 1u);
+          umma_commit(pv_done(t & 1));
+          umma_commit(v_empty(st));
+          ++pv_issued;
+          did = true;
         }
         if (end_at >= 0 && pv_issued == s_issued) break;
         // the clock is only read while idle: from the 256th empty poll on
