@@ -20,16 +20,24 @@
 //     P^T is block-diagonal: row h*T + t holds p only in the columns of head h,
 //     so each query head accumulates only the V rows of its own KV head.
 //
-// Per CTA (224 threads, one CTA per SM): warp 0 loads Q rows when a sequence
-// segment starts and the K box of every stage, warp 6 the V box (separate K and
-// V rings of up to three 32 KB stages each, so V never holds up the next S),
-// warp 1 owns TMEM and issues the MMAs, warps 2-5 run the softmax with
-// one thread per row: the T rows of a KV head sit in one warp, so the per-head
-// stage maximum and the row sums are warp shuffles. The running maximum is
-// rescaled lazily (only when it grows by more than 2^8), and the rare rescale of
-// O^T is broadcast through shared memory with one barrier per stage. Rows of
+// Per CTA (one CTA per SM): warp 0 loads Q rows when a sequence segment starts
+// and the K box of every stage, warp 6 the V box (separate K and V rings of up
+// to three 32 KB stages each, so V never holds up the next S), warp 1 owns
+// TMEM and issues the MMAs, warps 2-5 run the softmax with one thread per row:
+// the T rows of a KV head sit in one warp. A segment's first stage fixes each
+// head's reference maximum (warp shuffles); later stages only test whether a
+// score exceeds it by more than 2^8, and the four softmax warps meet once per
+// stage on one hardware barrier that ORs that test over their threads: only
+// when it fires do they compute new maxima and rescale O^T together. Rows of
 // tokens outside the segment are masked and their V rows zeroed, so unwritten
 // cache slots never reach the PV MMA.
+//
+// A shared-memory access (a barrier probe, a load) that the MMA thread issues
+// behind its own MMAs waits until the tensor core has taken them. With bf16
+// caches (256 threads) warp 7 therefore does all the barrier polling and hands
+// the MMA warp commands through a counting hardware barrier; with fp8 caches
+// (480 threads: two converter warpgroups added) the MMA thread polls itself,
+// reading every barrier of a round before issuing that round's MMAs.
 //
 // CTA b owns the flat token range [bW, (b+1)W) of the concatenated contexts
 // (all heads), exactly like the split kernel in decode.cu, and leaves the same
@@ -52,8 +60,9 @@ constexpr int kRows = 128;            // MMA M: rows of a stage (T tokens x Hkv 
 constexpr int kHD = 128;
 constexpr int kRegion = 16384;        // 128 rows x 128 B (one 64-dim half)
 constexpr int kKVBytes = 2 * kRegion;
-constexpr int kThreads = 224;  // K producer, MMA, 4 softmax warps, V producer
-// fp8 caches add two converter warpgroups (warps 7-10: K, 11-14: V)
+constexpr int kThreads = 256;  // K producer, MMA, 4 softmax warps, V producer, MMA scheduler
+// fp8 caches add two converter warpgroups (warps 7-10: K, 11-14: V); their MMA
+// warp polls its barriers itself (no scheduler warp)
 constexpr int kThreadsF8 = 480;
 constexpr int kRawCodes = 16384;      // one fp8 stage: 128 rows x 128 one-byte codes
 constexpr int kRawStage = 17408;      // codes + 128 fp32 row scales, padded to 1024 B
@@ -63,6 +72,9 @@ constexpr int kMaxG = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.f;
 constexpr int kSoftmaxBarrier = 1;    // named barrier of the four softmax warps (0 is __syncthreads)
+constexpr int kIssueBarrier = 2;      // named barrier of the MMA warp and the MMA scheduler warp
+// commands from the scheduler to the MMA warp (a count from 0 to 31)
+enum : int { kCmdPV = 1, kCmdPVFirst = 2, kCmdS = 4, kCmdFinish = 8, kCmdAbort = 16 };
 
 enum : int { kFirst = 1, kLast = 2, kEnd = 4 };
 
@@ -475,8 +487,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   (j / S) & 1, nullptr);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (F8 && warp == 1) {
+    // ------------------------------------------- MMA issuer, fp8 (self-polling)
+    // With 15 warps every SM sub-partition already runs three or four busy
+    // warps, and a separate scheduler warp measured slower than this thread
+    // polling its barriers itself (probes first, then the round's MMAs).
     if (lane == 0) {
       // fp8 caches: both operands of both MMAs are f16 (A/B format fields 0)
       constexpr uint32_t kFmt = F8 ? ~((1u << 7) | (1u << 10)) : ~0u;
@@ -567,7 +582,129 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (pv_issued > 0) mbar_wait(pv_done((pv_issued - 1) & 1), ((pv_issued - 1) >> 1) & 1, nullptr);
     }
     __syncwarp();
-  } else if (F8 && warp >= 7) {
+  } else if (!F8 && warp == 1) {
+    // ------------------------------------------- MMA issuer, bf16 (commanded)
+    // Issues what the scheduler warp tells it, in a fixed order: S(0), S(1),
+    // then per stage t: PV(t) and S(t + 2). A shared-memory access this thread
+    // issued behind its own MMAs would wait until the tensor core has taken
+    // them, so it makes none: it learns each command at a hardware barrier
+    // that sums a predicate over the scheduler's lanes.
+    constexpr uint32_t kFmt = F8 ? ~((1u << 7) | (1u << 10)) : ~0u;  // fp8: f16 operands
+    const uint32_t idesc_s = umma_idesc_bf16(kRows, N, false) & kFmt;
+    const uint32_t idesc_pv = (umma_idesc_bf16(kHD, N, false) | (1u << 15)) & kFmt;  // A (V) MN-major
+    int s_issued = 0, pv_issued = 0;
+    for (;;) {
+      const int cmd = bar_red_popc(kIssueBarrier, 64, false);
+      if (cmd & (kCmdFinish | kCmdAbort)) break;
+      if (lane == 0) {
+        if (cmd & kCmdPV) {
+          const int t = pv_issued, st = t % S;
+          const bool first = (cmd & kCmdPVFirst) != 0;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk)
+            umma_bf16(tmem_o, desc_v(sV + st * kKVBytes, kk), desc_k(sP + (t & 1) * 2 * small, kk, small),
+                      idesc_pv, (first && kk == 0) ? 0u : 1u);
+          umma_commit(pv_done(t & 1));
+          umma_commit(v_empty(st));
+        }
+        if (cmd & kCmdS) {
+          const int j = s_issued, sj = j % S, bj = j & 1;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kHD / 16; ++kk) {
+            if (F8)
+              umma_tmem_a(tmem_s(bj), tmem + kK0 + sj * 64 + kk * 8, desc_k(sQ, kk, small), idesc_s,
+                          kk > 0 ? 1u : 0u);
+            else
+              umma_bf16(tmem_s(bj), desc_k(sK + sj * kKVBytes, kk, kRegion), desc_k(sQ, kk, small),
+                        idesc_s, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full(bj));
+        }
+      }
+      if (cmd & kCmdPV) ++pv_issued;
+      if (cmd & kCmdS) ++s_issued;
+    }
+    // every MMA issued completes before TMEM is freed
+    if (lane == 0) {
+      if (s_issued > 0) mbar_wait(s_full((s_issued - 1) & 1), ((s_issued - 1) >> 1) & 1, nullptr);
+      if (pv_issued > 0) mbar_wait(pv_done((pv_issued - 1) & 1), ((pv_issued - 1) >> 1) & 1, nullptr);
+    }
+    __syncwarp();
+  } else if (!F8 && warp == NT / 32 - 1) {
+    // --------------------------------------------------------- MMA scheduler
+    // Polls the inputs of the MMA warp's next groups and hands them over as
+    // commands: PV(t) once V(t) and P(t) are ready; S(j) once K(j) is ready
+    // and the softmax warps have read S^T[j & 1] (S(j - 2)), which S(j)
+    // overwrites. Both may go in one command, PV first.
+    // The walk ends at the stage whose descriptor carries kEnd.
+    auto send = [&](int cmd) { bar_red_popc(kIssueBarrier, 64, lane < cmd); };
+    int t_pv = 0, j_s = 0;      // next PV, next S
+    int n = -1;                 // number of stages, once the end has been seen
+    uint32_t first_of = 0;      // bit t & 31: kFirst of stage t
+    bool ok = true;
+    unsigned long long idle_since = 0;
+    for (uint32_t idle = 0;;) {
+      int cmd = 0, done = 0;
+      if (lane == 0) {
+        bool pv = false;
+        if (t_pv < j_s) {
+          const bool v_ready = mbar_test_wait(v_full(t_pv % S), (t_pv / S) & 1);
+          const bool p_ready = mbar_test_wait(p_full(t_pv & 1), (t_pv >> 1) & 1);
+          pv = v_ready && p_ready;
+        }
+        const int pv_after = t_pv + (pv ? 1 : 0);
+        bool sv = false;
+        // at most two S ahead of the PVs: S(j) writes the S^T buffer of S(j - 2)
+        if (n < 0 && j_s - pv_after < 3 && mbar_test_wait(k_full(j_s % S), (j_s / S) & 1) &&
+            (j_s < 2 || mbar_test_wait(s_free(j_s & 1), ((j_s - 2) >> 1) & 1))) {
+          const int flags = desc[j_s % S].flags;
+          if (flags & kEnd) {
+            n = j_s;
+          } else {
+            sv = true;
+            first_of = (first_of & ~(1u << (j_s & 31))) | ((flags & kFirst) ? 1u << (j_s & 31) : 0u);
+          }
+        }
+        if (pv) cmd |= kCmdPV | (((first_of >> (t_pv & 31)) & 1u) ? kCmdPVFirst : 0);
+        if (sv) cmd |= kCmdS;
+        done = (n >= 0 && pv_after == n) ? 1 : 0;
+        // nothing to hand over: sleep on the barrier that usually completes
+        // next (P of the oldest pending PV, else the next K stage) instead of
+        // spinning, which would take issue slots from the warps sharing this
+        // scheduler's SM sub-partition
+        if (!cmd && !done) {
+          if (t_pv < j_s) mbar_try_wait(p_full(t_pv & 1), (t_pv >> 1) & 1);
+          else if (n < 0) mbar_try_wait(k_full(j_s % S), (j_s / S) & 1);
+        }
+      }
+      cmd = __shfl_sync(0xffffffffu, cmd, 0);
+      done = __shfl_sync(0xffffffffu, done, 0);
+      n = __shfl_sync(0xffffffffu, n, 0);
+      if (cmd) {
+        send(cmd);
+        if (cmd & kCmdPV) ++t_pv;
+        if (cmd & kCmdS) ++j_s;
+        idle = 0;
+      }
+      if (done) break;
+      if (!cmd && (++idle & 255u) == 0) {
+        int stop = 0;
+        if (lane == 0) {
+          const unsigned long long now = global_timer_ns();
+          if (idle == 256u) idle_since = now;
+          else if (*abort_flag || now - idle_since > kWaitTimeoutNs) stop = 1;
+        }
+        if (__shfl_sync(0xffffffffu, stop, 0)) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (!ok) fail();
+    send(ok ? kCmdFinish : kCmdAbort);
+  } else if (F8 && warp >= 7 && warp < 15) {
     // ------------------------------------------------------------ converters
     // Warps 7-10 expand each raw K stage, warps 11-14 each raw V stage, one
     // 128-code row per thread, from E4M3 into the f16 operand layout (and, at
@@ -687,10 +824,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
+        // S^T[j & 1] has been read (S(j + 2) may overwrite it); S(j) has
+        // completed, so K(j) is no longer read, and the descriptor and the K
+        // scales of this stage have been read too: the K slot is free
         if (lane == 0) {
           mbar_arrive(s_free(buf));
-          // S(j) has completed, so K(j) is no longer read; the descriptor and
-          // the K scales of this stage have been read too: the K slot is free
           mbar_arrive(k_empty(s));
         }
 #pragma unroll

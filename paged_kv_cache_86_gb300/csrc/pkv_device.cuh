@@ -174,6 +174,17 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool v) {
   return r != 0;
 }
 
+// Hardware barrier that returns how many participating threads passed true.
+__device__ __forceinline__ int bar_red_popc(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.popc.u32 %0, %2, %3, q;\n\t}"
+      : "=r"(r) : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads) : "memory");
+  return static_cast<int>(r);
+}
+
 __device__ __forceinline__ void bar_sync(int id, int nthreads) {
   asm volatile("barrier.cta.sync.aligned %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
