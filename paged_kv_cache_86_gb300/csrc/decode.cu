@@ -98,6 +98,8 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // kernel), num_kv_heads when it covers (KV head, token) pairs (tcgen05 kernel).
 // Decode step: the newest token row of each sequence, written by the plan
 // launch's CTAs 1.. while CTA 0 computes the prefix sums (key == nullptr: none).
+constexpr int kStoreSeqsPerCta = 8;   // decode step: new rows written by four warps per sequence
+
 struct NewTokens {
   const uint4 *key;
   const uint4 *value;
@@ -124,12 +126,13 @@ decode_plan_kernel(const int32_t *__restrict__ context_lens, int num_seqs, int m
   // it may start its prologue now and waits for this grid before reading
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (blockIdx.x > 0) {
-    // Decode step: one warp per sequence writes its newest token at logical
-    // position n - 1, n = context_lens[i] clamped to [0, max_context_len] as
-    // below (n = 0 writes nothing): row (n-1) % bs of block
-    // block_tables[i][(n-1) / bs]. The decode kernel that reads the cache is
-    // the next launch on the stream.
-    const int i = (blockIdx.x - 1) * 32 + warp;
+    // Decode step: four warps per sequence (eight sequences per CTA, so the
+    // rows spread over many SMs) write its newest token at logical position
+    // n - 1, n = context_lens[i] clamped to [0, max_context_len] as below
+    // (n = 0 writes nothing): row (n-1) % bs of block block_tables[i][(n-1) / bs].
+    // The decode kernel that reads the cache is the next launch on the stream.
+    const int i = (blockIdx.x - 1) * kStoreSeqsPerCta + (warp >> 2);
+    const int part = warp & 3;
     if (i >= num_seqs) return;
     int n = context_lens[i];
     n = n < 0 ? 0 : (n > max_context_len ? max_context_len : n);
@@ -141,9 +144,11 @@ decode_plan_kernel(const int32_t *__restrict__ context_lens, int num_seqs, int m
       return;
     }
     const int64_t row = static_cast<int64_t>(blk) * nt.block_size + pos % nt.block_size;
-    for (int v = lane; v < nt.row_vecs; v += 32) {
-      nt.k_cache[row * nt.row_vecs + v] = __ldg(nt.key + i * nt.key_stride_vecs + v);
-      nt.v_cache[row * nt.row_vecs + v] = __ldg(nt.value + i * nt.value_stride_vecs + v);
+    for (int v = part * 32 + lane; v < nt.row_vecs; v += 128) {
+      const uint4 kv = __ldg(nt.key + i * nt.key_stride_vecs + v);
+      const uint4 vv = __ldg(nt.value + i * nt.value_stride_vecs + v);
+      nt.k_cache[row * nt.row_vecs + v] = kv;
+      nt.v_cache[row * nt.row_vecs + v] = vv;
     }
     return;
   }
@@ -734,7 +739,7 @@ cudaError_t launch_plan(const DecodeArgs &a, int grid, int units_per_token, int 
     nt.row_vecs = a.num_kv_heads * (kHeadDim / 8);
     nt.key_stride_vecs = a.key_stride / 8;
     nt.value_stride_vecs = a.value_stride / 8;
-    ctas += static_cast<unsigned>((a.num_seqs + 31) / 32);
+    ctas += static_cast<unsigned>((a.num_seqs + kStoreSeqsPerCta - 1) / kStoreSeqsPerCta);
   }
   decode_plan_kernel<<<ctas, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len,
                                                 grid, units_per_token, min_range, ws, a.err, nt);
