@@ -324,6 +324,38 @@ pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void 
   uint32_t *err = pkv::device_error_word(&e);
   if (!err) return PKV_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the prefill chunks D..S-1 (their query rows are absolute offsets in cu_seqlens_q)
+  pkv::PrefillArgs pa;
+  pa.out = out;
+  pa.q = q;
+  pa.k_cache = k_cache;
+  pa.v_cache = v_cache;
+  pa.cu_seqlens_q = cu_seqlens_q + num_decode_seqs;
+  pa.cu_seqlens_k = cu_seqlens_k + num_decode_seqs;
+  pa.max_seqlen_q = max_seqlen_q;
+  pa.max_seqlen_k = max_seqlen_k;
+  pa.block_tables = block_tables + static_cast<int64_t>(num_decode_seqs) * max_blocks_per_seq;
+  pa.max_blocks_per_seq = max_blocks_per_seq;
+  pa.num_seqs = num_prefill;
+  pa.total_q = total_q;
+  pa.num_q_heads = num_q_heads;
+  pa.num_kv_heads = num_kv_heads;
+  pa.block_size = block_size;
+  pa.num_blocks = num_blocks;
+  pa.scale = scale;
+  pa.causal = 1;
+  pa.err = err;
+  pa.workspace = static_cast<uint8_t *>(workspace) + lens_bytes + dec_aligned;
+  // With the all-heads decode kernel the prefill is launched between it and
+  // the combine, overlapping its tail: it reads only the caches, which the
+  // store below has finished writing before the decode's first kernel starts.
+  const bool interleave = num_prefill > 0 && num_decode_seqs > 0 && plan.kind == 3 &&
+                          pkv::prefill_pp_supported(num_q_heads, num_kv_heads, block_size);
+  if (interleave) {
+    if ((e = cudaMemsetAsync(pa.workspace, 0, sizeof(uint32_t), st)) != cudaSuccess) return PKV_ERR_CUDA;
+    pa.ticket_zeroed = true;
+    pa.overlap_previous = true;
+  }
   // 1. every new token of the batch (decode tokens and chunk tokens) into the cache
   e = pkv::launch_store_kvcache(key, value, k_cache, v_cache, slot_mapping, total_q,
                                 static_cast<int32_t>(row), key_token_stride, value_token_stride,
@@ -353,33 +385,13 @@ pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void 
     a.workspace = static_cast<uint8_t *>(workspace) + lens_bytes;
     a.workspace_bytes = dec_bytes;
     a.err = err;
+    a.interleave = interleave ? &pa : nullptr;
     if ((e = pkv::launch_paged_decode(a, plan, st)) != cudaSuccess) return PKV_ERR_CUDA;
   }
-  // 3. the prefill chunks D..S-1 (their query rows are absolute offsets in cu_seqlens_q)
-  if (num_prefill > 0) {
-    pkv::PrefillArgs a;
-    a.out = out;
-    a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
-    a.cu_seqlens_q = cu_seqlens_q + num_decode_seqs;
-    a.cu_seqlens_k = cu_seqlens_k + num_decode_seqs;
-    a.max_seqlen_q = max_seqlen_q;
-    a.max_seqlen_k = max_seqlen_k;
-    a.block_tables = block_tables + static_cast<int64_t>(num_decode_seqs) * max_blocks_per_seq;
-    a.max_blocks_per_seq = max_blocks_per_seq;
-    a.num_seqs = num_prefill;
-    a.total_q = total_q;
-    a.num_q_heads = num_q_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.block_size = block_size;
-    a.num_blocks = num_blocks;
-    a.scale = scale;
-    a.causal = 1;
-    a.err = err;
-    a.workspace = static_cast<uint8_t *>(workspace) + lens_bytes + dec_aligned;
-    if ((e = pkv::launch_paged_prefill(a, st)) != cudaSuccess) return PKV_ERR_CUDA;
-  }
+  // 3. the prefill chunks, unless they ran between the decode kernels
+  if (num_prefill > 0 && !interleave &&
+      (e = pkv::launch_paged_prefill(pa, st)) != cudaSuccess)
+    return PKV_ERR_CUDA;
   return PKV_OK;
 }
 

@@ -835,6 +835,11 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
     if ((e = launch_decode_tcg(a, grid, reinterpret_cast<float2 *>(ws + lay.ml),
                                reinterpret_cast<float *>(ws + lay.o), stream)) != cudaSuccess)
       return e;
+    // mixed batch: the prefill runs on the SMs the attention kernel leaves as
+    // its CTAs finish; the combine below waits for the prefill, which waits
+    // for the attention kernel before it exits
+    if (a.interleave != nullptr && (e = launch_paged_prefill(*a.interleave, stream)) != cudaSuccess)
+      return e;
   } else if (plan.kind == 2) {
     if ((e = launch_plan(a, grid, a.num_kv_heads, 128, ws, stream)) != cudaSuccess) return e;
     const size_t ml = align256(256 + sizeof(int) * (size_t(a.num_seqs) + 1));

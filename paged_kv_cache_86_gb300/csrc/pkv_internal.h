@@ -62,6 +62,10 @@ struct DecodeArgs {
   const void *value_new = nullptr;
   int64_t key_stride = 0;
   int64_t value_stride = 0;
+  // mixed batch: a prefill launched between the tcgen05 attention kernel and
+  // the combine, so that it fills the SMs the attention kernel's tail leaves
+  // (nullptr otherwise)
+  const struct PrefillArgs *interleave = nullptr;
   // fp8 E4M3 caches (uint8 codes) with fp32 row scales [NB * bs, Hkv]
   bool fp8 = false;
   const float *k_scales = nullptr;
@@ -126,6 +130,13 @@ struct PrefillArgs {
   // kPrefillWorkspace bytes of device scratch (the work ticket of the
   // persistent kernel), 256-byte aligned
   void *workspace = nullptr;
+  // the caller has zeroed the work ticket already (earlier on the stream)
+  bool ticket_zeroed = false;
+  // launch as a programmatic dependent of the previous kernel on the stream
+  // without waiting for it: the caller guarantees that the prefill reads
+  // nothing that kernel writes. The kernel still waits for it before it
+  // exits, so a later dependent sees both finished.
+  bool overlap_previous = false;
 };
 
 constexpr size_t kPrefillWorkspace = 256;

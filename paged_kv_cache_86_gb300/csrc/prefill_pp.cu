@@ -583,6 +583,10 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // launched as a programmatic dependent that overlaps the previous kernel:
+  // finish only after it has, so that the next dependent sees both done (a
+  // no-op for an ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -661,7 +665,8 @@ cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
   p.q_tiles = (a.max_seqlen_q + kTile - 1) / kTile;
   p.ticket = static_cast<uint32_t *>(a.workspace);
   if (p.ticket == nullptr) return cudaErrorInvalidValue;
-  if (cudaError_t me = cudaMemsetAsync(p.ticket, 0, sizeof(uint32_t), stream)) return me;
+  if (!a.ticket_zeroed)
+    if (cudaError_t me = cudaMemsetAsync(p.ticket, 0, sizeof(uint32_t), stream)) return me;
   const long long n_items = static_cast<long long>(p.q_tiles) * (a.num_q_heads / 2) * a.num_seqs;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -669,8 +674,21 @@ cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
   const int sms = sm_count(dev);
   if (sms <= 0) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  prefill_pp_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  if (!a.overlap_previous) {
+    prefill_pp_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_pp_kernel, tq, tk, tv, p);
 }
 
 }  // namespace pkv
