@@ -360,6 +360,19 @@ pkv_status pkv_get_device_errors(void *stream, uint32_t *bits);
 
 const char *pkv_status_string(pkv_status status);
 
+/* pkv_selftest_bounded_wait: an on-GPU check of the failure path the kernels
+ * rely on (no fault, trap or endless loop is involved). One CTA of two warps
+ * runs eight steps and meets once per step on an OR-reducing hardware barrier;
+ * in step fail_step warp 1 waits 5 ms on an mbarrier that nothing arrives on.
+ * The wait must give up, raise PKV_DEVERR_TIMEOUT in the device error word,
+ * and both warps must leave the loop in that step.
+ *   result  device int32[4], zeroed by the caller: the step in which warp 0
+ *           and warp 1 left, 1 if the timeout was reported, the number of
+ *           steps both completed. fail_step >= 8: no wait runs out.
+ * Asynchronous on `stream`; read result and pkv_get_device_errors after it.
+ */
+pkv_status pkv_selftest_bounded_wait(int32_t fail_step, int32_t *result, void *stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t pkv_version(void);
 

@@ -76,12 +76,14 @@ def load(path: str = LIB_PATH):
                                           i32, i32, i32, i32, i32, f32, i32, vp, sz, ctypes.c_int,
                                           vp]
         lib.pkv_get_device_errors.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.pkv_selftest_bounded_wait.argtypes = [i32, vp, vp]
         lib.pkv_status_string.argtypes = [ctypes.c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_version.restype = i32
         for name in ("pkv_store_kvcache", "pkv_paged_decode", "pkv_decode_step",
                      "pkv_paged_prefill", "pkv_copy_blocks", "pkv_store_kvcache_fp8",
-                     "pkv_paged_decode_fp8", "pkv_mixed_step", "pkv_get_device_errors"):
+                     "pkv_paged_decode_fp8", "pkv_mixed_step", "pkv_get_device_errors",
+                     "pkv_selftest_bounded_wait"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -411,6 +413,17 @@ def paged_prefill(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables,
                                  ws_ptr, ws_bytes, PKV_BF16, _stream(q, stream)),
            "pkv_paged_prefill")
     return out
+
+
+def selftest_bounded_wait(fail_step: int, stream=None) -> list:
+    """Run the library's on-GPU failure-path check (see pkv.h); returns
+    [step warp 0 left, step warp 1 left, timeout reported, steps completed]."""
+    lib = load()
+    res = torch.zeros(4, dtype=torch.int32, device="cuda")
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib.pkv_selftest_bounded_wait(int(fail_step), _ptr(res), ctypes.c_void_p(s.cuda_stream)),
+           "pkv_selftest_bounded_wait")
+    return res.cpu().tolist()
 
 
 def get_device_errors(stream=None) -> int:

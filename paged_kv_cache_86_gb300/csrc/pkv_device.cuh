@@ -143,19 +143,24 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed. Gives up (returns
-// false) when *abort becomes non-zero or after the timeout; never spins forever.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          const volatile int *abort) {
+// false) when *abort becomes non-zero or after limit_ns; never spins forever.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, const volatile int *abort,
+                                              unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t polls = 1; polls < kWaitMaxPolls; ++polls) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((polls & 63u) == 0) {
       if (abort != nullptr && *abort) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
   return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          const volatile int *abort) {
+  return mbar_wait_for(bar, parity, abort, kWaitTimeoutNs);
 }
 
 // ------------------------------------------------------ named barriers --
