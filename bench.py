@@ -57,6 +57,9 @@ def parse():
                     help="warm-up and timed steps only: no per-op, e2e, clocks or CPU legs")
     ap.add_argument("--only-prefill", action="store_true",
                     help="time only the chunked-prefill row (store + prefill), for profiling")
+    ap.add_argument("--only-row", choices=["fp8", "copy", "mixed"], default=None,
+                    help="time only the fp8-decode, block-copy or mixed-round row, for profiling "
+                         "(--num-seqs applies to the fp8 row)")
     return ap.parse_args()
 
 
@@ -444,14 +447,14 @@ def fp8_decode_bytes(w) -> int:
     return kv + qo + tables
 
 
-def measure_fp8_decode(device, steps):
+def measure_fp8_decode(device, steps, num_seqs=None):
     """The fp8 KV row: the 512-sequence decode batch over an fp8 E4M3 cache
     (per token-head scales): the quantizing store of the 512 new tokens, then
     pkv_paged_decode_fp8, each timed with CUDA events."""
     import torch
     import paged_kv_cache_86_gb300 as pkv
     from paged_kv_cache_86_gb300 import workloads as W
-    w = make_workload("decode_512seq", fill="device")
+    w = make_workload("decode_512seq", fill="device", num_seqs=num_seqs)
     t = {k: v.to(device) for k, v in w.tensors.items() if k in ("q", "key", "value")}
     kc, ks = W.fp8_pool(w.num_blocks, w.block_size, w.num_kv_heads, w.seed * 16 + 7, device=device)
     vc, vs = W.fp8_pool(w.num_blocks, w.block_size, w.num_kv_heads, w.seed * 16 + 8, device=device)
@@ -493,7 +496,7 @@ def measure_fp8_decode(device, steps):
             "algorithmic_bytes_per_launch": nbytes,
             "gbs": nbytes / (decode_ms * 1e-3) / 1e9,
             "frac_of_hbm": nbytes / (decode_ms * 1e-3) / 1e9 / hpeak,
-            "l2": "inputs larger than L2 (1.2 GB of codes per launch)"}
+            "l2": f"inputs larger than L2 ({nbytes / 1e9:.2f} GB of codes and scales per launch)"}
 
 
 def measure_mixed(device, steps):
@@ -535,22 +538,15 @@ def measure_mixed(device, steps):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
-        times = []
-        for _ in range(steps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            times.append(a.elapsed_time(b))
-        res[name] = statistics.median(times)
+        res[name] = timed_after_clean_flush(fn, steps, device)
     if pkv.get_device_errors() != 0:
         raise RuntimeError("device-side range check fired in the mixed-batch measurement")
     tokens = int(w.num_q_rows)
     return {"workload": w.name, "scheduled_tokens": tokens, "ms": res["mixed_step"],
             "tokens_per_s": tokens / (res["mixed_step"] * 1e-3),
             "ms_all_through_prefill_kernel": res["store_plus_prefill_kernel_for_all"],
-            "l2": "K/V of the round larger than L2 (~1 GB); median of launches"}
+            "l2": "K/V of the round larger than L2 (~1 GB); each launch after a clean 256 MiB "
+                  "L2 refill; median of launches"}
 
 
 def measure_copy_blocks(device, steps):
@@ -566,27 +562,20 @@ def measure_copy_blocks(device, steps):
     perm = torch.randperm(nb, generator=torch.Generator().manual_seed(86010))
     src = perm[:pairs].to(torch.int32).to(device)
     dst = perm[pairs:2 * pairs].to(torch.int32).to(device)
-    stream = torch.cuda.current_stream(device)
     for _ in range(3):
         pkv.copy_blocks(kc, vc, src, dst)
     torch.cuda.synchronize()
-    times = []
-    for _ in range(steps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        pkv.copy_blocks(kc, vc, src, dst)
-        b.record(stream)
-        torch.cuda.synchronize()
-        times.append(a.elapsed_time(b))
+    ms = timed_after_clean_flush(lambda: pkv.copy_blocks(kc, vc, src, dst), steps, device)
     if pkv.get_device_errors() != 0:
         raise RuntimeError("device-side range check fired in the block-copy measurement")
-    ms = statistics.median(times)
     nbytes = pairs * 2 * 2 * bs * hkv * d * 2      # K and V, read and write
     hpeak, _ = measured_peaks()
     return {"workload": f"copy_{pairs}_blocks_bs{bs}_hkv{hkv}", "bytes_per_launch": nbytes,
             "ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
             "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hpeak,
-            "l2": "512 MiB per launch, larger than L2; median of launches"}
+            "l2": "512 MiB per launch, larger than L2; each launch after a clean 256 MiB L2 refill; "
+                  "median of launches; up to one L2 of the copy's writes (ncu: ~50 MB) is still "
+                  "being written back when the end event fires"}
 
 
 def prefill_flops(w) -> int:
@@ -596,6 +585,28 @@ def prefill_flops(w) -> int:
     k_lens = np.diff(w.cu_seqlens_k).astype(np.int64)
     vis = sum(int(((k - q) + np.arange(1, q + 1)).sum()) for q, k in zip(q_lens, k_lens))
     return 4 * w.head_dim * w.num_q_heads * vis
+
+
+def timed_after_clean_flush(fn, steps, device):
+    """Median CUDA-event time of fn() over `steps` launches, each started right
+    after L2 has been refilled with clean, unrelated lines (256 MiB written, then
+    256 MiB read). The flush also keeps the GPU busy while the host submits fn(),
+    so the events time the GPU work, not the host-side launch latency."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush_rd = torch.ones(64 << 20, dtype=torch.float32, device=device)
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        flush_rd.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times)
 
 
 def measure_prefill(args, device, steps):
@@ -714,6 +725,15 @@ def main():
     if args.only_prefill:
         torch.cuda.set_device(device)
         res = {"prefill_row": measure_prefill(args, device, steps=max(1, args.steps))}
+    elif args.only_row is not None:
+        torch.cuda.set_device(device)
+        steps = max(1, args.steps)
+        if args.only_row == "fp8":
+            res = {"fp8_decode_row": measure_fp8_decode(device, steps, num_seqs=args.num_seqs)}
+        elif args.only_row == "copy":
+            res = {"copy_blocks_row": measure_copy_blocks(device, steps)}
+        else:
+            res = {"mixed_batch_row": measure_mixed(device, steps)}
     else:
         res = run_pkv(args, rank, world, device)
     if rank == 0:
