@@ -73,9 +73,9 @@ __device__ __forceinline__ uint32_t quantize4_e4m3(uint2 bits, float inv) {
   return static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
 }
 
-__device__ __forceinline__ void quantize_row_e4m3(const uint2 *src, uint32_t *codes, float *scale,
+// One 128-element row per warp, four elements per lane (`bits`, already loaded).
+__device__ __forceinline__ void quantize_row_e4m3(const uint2 bits, uint32_t *codes, float *scale,
                                                   int lane) {
-  const uint2 bits = __ldg(src + lane);
   const float2 lo = bf16x2_to_float2(bits.x), hi = bf16x2_to_float2(bits.y);
   float amax = fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(hi.x), fabsf(hi.y)));
 #pragma unroll
@@ -98,22 +98,23 @@ store_kvcache_fp8_kernel(const __nv_bfloat16 *__restrict__ key,
                          float *__restrict__ v_scales, const int32_t *__restrict__ slot_mapping,
                          int32_t num_tokens, int32_t num_kv_heads, int64_t key_stride,
                          int64_t value_stride, int64_t num_slots, uint32_t *err) {
+  // one warp per (token, KV head): its K row and its V row, both loads first
   const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t t = gw / num_kv_heads;
+  const int h = static_cast<int>(gw - t * num_kv_heads);
   if (t >= num_tokens) return;
   const int64_t slot = __ldg(slot_mapping + t);
   if (slot < 0) return;  // padded token
   if (slot >= num_slots) {
-    if (lane == 0) raise_error(err, PKV_DEVERR_SLOT);
+    if (lane == 0 && h == 0) raise_error(err, PKV_DEVERR_SLOT);
     return;
   }
-  for (int h = 0; h < num_kv_heads; ++h) {
-    const int64_t row = slot * num_kv_heads + h;
-    quantize_row_e4m3(reinterpret_cast<const uint2 *>(key + t * key_stride + h * 128),
-                      reinterpret_cast<uint32_t *>(k_cache + row * 128), k_scales + row, lane);
-    quantize_row_e4m3(reinterpret_cast<const uint2 *>(value + t * value_stride + h * 128),
-                      reinterpret_cast<uint32_t *>(v_cache + row * 128), v_scales + row, lane);
-  }
+  const int64_t row = slot * num_kv_heads + h;
+  const uint2 kb = __ldg(reinterpret_cast<const uint2 *>(key + t * key_stride + h * 128) + lane);
+  const uint2 vb = __ldg(reinterpret_cast<const uint2 *>(value + t * value_stride + h * 128) + lane);
+  quantize_row_e4m3(kb, reinterpret_cast<uint32_t *>(k_cache + row * 128), k_scales + row, lane);
+  quantize_row_e4m3(vb, reinterpret_cast<uint32_t *>(v_cache + row * 128), v_scales + row, lane);
 }
 
 }  // namespace
@@ -124,7 +125,8 @@ cudaError_t launch_store_kvcache_fp8(const void *key, const void *value, void *k
                                      int32_t num_kv_heads, int64_t key_stride, int64_t value_stride,
                                      int64_t num_slots, uint32_t *err, cudaStream_t stream) {
   if (num_tokens == 0) return cudaSuccess;
-  const unsigned grid = static_cast<unsigned>((num_tokens + kWarpsPerCta - 1) / kWarpsPerCta);
+  const int64_t warps = static_cast<int64_t>(num_tokens) * num_kv_heads;
+  const unsigned grid = static_cast<unsigned>((warps + kWarpsPerCta - 1) / kWarpsPerCta);
   store_kvcache_fp8_kernel<<<grid, kWarpsPerCta * 32, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(key), static_cast<const __nv_bfloat16 *>(value),
       static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), k_scales, v_scales,
