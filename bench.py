@@ -450,7 +450,8 @@ def fp8_decode_bytes(w) -> int:
 def measure_fp8_decode(device, steps, num_seqs=None):
     """The fp8 KV row: the 512-sequence decode batch over an fp8 E4M3 cache
     (per token-head scales): the quantizing store of the 512 new tokens, then
-    pkv_paged_decode_fp8, each timed with CUDA events."""
+    pkv_paged_decode_fp8, each timed with CUDA events; and the same step as one
+    pkv_decode_step_fp8 call."""
     import torch
     import paged_kv_cache_86_gb300 as pkv
     from paged_kv_cache_86_gb300 import workloads as W
@@ -488,10 +489,32 @@ def measure_fp8_decode(device, steps, num_seqs=None):
         raise RuntimeError("device-side range check fired in the fp8 measurement")
     store_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
     decode_ms = statistics.mean(b.elapsed_time(c) for _, b, c in evs)
+    # the same step as one call: every sequence of the batch is non-empty, so
+    # new-token row i is sequence i's
+    assert (w.context_lens > 0).all()
+
+    def fused():
+        pkv.decode_step_fp8(t["q"], t["key"], t["value"], kc, vc, ks, vs, bt, cl, w.scale,
+                            out=out, workspace=ws)
+
+    for _ in range(3):
+        fused()
+    torch.cuda.synchronize()
+    fevs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(steps)]
+    for a, b in fevs:
+        a.record(stream)
+        fused()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if pkv.get_device_errors() != 0:
+        raise RuntimeError("device-side range check fired in the fp8 step measurement")
+    fused_ms = statistics.mean(a.elapsed_time(b) for a, b in fevs)
     hpeak, _ = measured_peaks()
     nbytes = fp8_decode_bytes(w)
     step_ms = store_ms + decode_ms
     return {"workload": w.name + "_fp8_e4m3", "decode_ms": decode_ms, "store_ms": store_ms,
+            "fused_step_ms": fused_ms,
+            "fused_step_tokens_per_s": w.num_seqs / (fused_ms * 1e-3),
             "tokens_per_s": w.num_seqs / (step_ms * 1e-3),
             "algorithmic_bytes_per_launch": nbytes,
             "gbs": nbytes / (decode_ms * 1e-3) / 1e9,

@@ -16,7 +16,8 @@
  *   pkv_paged_prefill  varlen query chunks (cu_seqlens_q) over their cached
  *                      prefix plus themselves (cu_seqlens_k), causal;
  *   pkv_copy_blocks    copy-on-write of shared cache blocks;
- *   *_fp8              the store and the decode over an fp8 E4M3 cache;
+ *   *_fp8              the store, the decode and the decode step over an fp8
+ *                      E4M3 cache;
  *   pkv_mixed_step     a batch of decode requests and prefill chunks.
  *
  * Cache layout. One layer's K cache and V cache are two separate arrays of
@@ -185,6 +186,27 @@ pkv_status pkv_paged_decode_fp8(void *out, const void *q,
                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                 int32_t block_size, int32_t num_blocks, float scale,
                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* pkv_decode_step_fp8: pkv_decode_step over fp8 caches -- each sequence's
+ * newest bf16 K/V row (key_new / value_new, as in pkv_decode_step) is quantized
+ * exactly as pkv_store_kvcache_fp8 quantizes it and written, codes and scales,
+ * at logical position min(context_lens[i], max_context_len) - 1; then
+ * pkv_paged_decode_fp8 runs. Equal, bit for bit, to pkv_store_kvcache_fp8 with
+ * those slots followed by pkv_paged_decode_fp8, in one call (the quantizing
+ * store runs inside the decode's first launch). Same shapes, workspace and
+ * errors as pkv_paged_decode_fp8.
+ */
+pkv_status pkv_decode_step_fp8(void *out, const void *q,
+                               const void *key_new, const void *value_new,
+                               int64_t key_token_stride, int64_t value_token_stride,
+                               void *k_cache, void *v_cache,
+                               float *k_scales, float *v_scales,
+                               const int32_t *block_tables, int32_t max_blocks_per_seq,
+                               const int32_t *context_lens, int32_t num_seqs,
+                               int32_t max_context_len,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int32_t num_blocks, float scale,
+                               void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------ block copy --
  * pkv_copy_blocks: for p < num_pairs, rows 0 .. num_rows[p]-1 of physical block

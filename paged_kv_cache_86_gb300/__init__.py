@@ -6,12 +6,14 @@ binding plus the seeded synthetic workload generator used by tests and the
 bench. Importing the package does not load the library; the first call does,
 and fails loudly if it has not been built.
 """
-from ._lib import (PkvError, copy_blocks, decode_step, decode_workspace_size, get_device_errors,
+from ._lib import (PkvError, copy_blocks, decode_step, decode_step_fp8, decode_workspace_size,
+                   get_device_errors,
                    load, mixed_step, mixed_workspace_size, paged_decode, paged_decode_fp8,
                    paged_prefill, prefill_workspace_size, selftest_bounded_wait, store_kvcache,
                    store_kvcache_fp8, version)
 
-__all__ = ["PkvError", "copy_blocks", "decode_step", "decode_workspace_size", "get_device_errors",
+__all__ = ["PkvError", "copy_blocks", "decode_step", "decode_step_fp8", "decode_workspace_size",
+           "get_device_errors",
            "load", "mixed_step", "mixed_workspace_size", "paged_decode", "paged_decode_fp8",
            "paged_prefill", "prefill_workspace_size", "selftest_bounded_wait", "store_kvcache",
            "store_kvcache_fp8", "version"]

@@ -63,6 +63,8 @@ def load(path: str = LIB_PATH):
                                               i64, i64, vp]
         lib.pkv_paged_decode_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
                                              i32, i32, i32, i32, f32, vp, sz, vp]
+        lib.pkv_decode_step_fp8.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, vp, i32, vp,
+                                            i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp]
         lib.pkv_mixed_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.pkv_mixed_workspace_size.restype = sz
         lib.pkv_mixed_step.argtypes = [vp, vp, vp, vp, vp, i64, i64, vp, vp, vp, vp, i32, i32, vp,
@@ -82,7 +84,8 @@ def load(path: str = LIB_PATH):
         lib.pkv_version.restype = i32
         for name in ("pkv_store_kvcache", "pkv_paged_decode", "pkv_decode_step",
                      "pkv_paged_prefill", "pkv_copy_blocks", "pkv_store_kvcache_fp8",
-                     "pkv_paged_decode_fp8", "pkv_mixed_step", "pkv_get_device_errors",
+                     "pkv_paged_decode_fp8", "pkv_decode_step_fp8", "pkv_mixed_step",
+                     "pkv_get_device_errors",
                      "pkv_selftest_bounded_wait"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -205,6 +208,52 @@ def paged_decode_fp8(q, k_cache, v_cache, k_scales, v_scales, block_tables, cont
                                     float(scale), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(),
                                     _stream(q, stream)), "pkv_paged_decode_fp8")
+    return out
+
+
+def decode_step_fp8(q, key_new, value_new, k_cache, v_cache, k_scales, v_scales, block_tables,
+                    context_lens, scale: float, max_context_len: int | None = None, out=None,
+                    workspace=None, stream=None) -> torch.Tensor:
+    """One decode step over fp8 E4M3 caches: quantizes each sequence's newest K/V row
+    (key_new / value_new [S, Hkv, 128] bf16, token rows may be strided) into logical
+    position context_lens[i] - 1 (codes and row scale), then decodes; returns out
+    [S, Hq, 128] bf16."""
+    lib = load()
+    _need(q, "q", torch.bfloat16, 3)
+    for t, n in ((key_new, "key_new"), (value_new, "value_new")):
+        _need(t, n, torch.bfloat16, 3)
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{n} rows must be contiguous [Hkv, D] blocks")
+    nb, bs, hkv, d = _need_fp8_cache(k_cache, v_cache, k_scales, v_scales)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    if not (q.is_contiguous() and block_tables.is_contiguous() and context_lens.is_contiguous()):
+        raise ValueError("decode tensors must be contiguous")
+    s, hq, dq = q.shape
+    if dq != d:
+        raise ValueError("q / cache head_dim mismatch")
+    if key_new.shape != (s, hkv, d) or value_new.shape != (s, hkv, d):
+        raise ValueError("key_new / value_new must be [S, Hkv, D]")
+    if block_tables.shape[0] != s or context_lens.shape[0] != s:
+        raise ValueError("metadata rows must equal the number of sequences")
+    mb = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = mb * bs
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
+    if out.shape != q.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like q")
+    need = decode_workspace_size(s, hq, hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check(lib.pkv_decode_step_fp8(_ptr(out), _ptr(q), _ptr(key_new), _ptr(value_new),
+                                   key_new.stride(0), value_new.stride(0), _ptr(k_cache),
+                                   _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+                                   _ptr(block_tables), mb, _ptr(context_lens), s,
+                                   int(max_context_len), hq, hkv, d, bs, nb, float(scale),
+                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(q, stream)), "pkv_decode_step_fp8")
     return out
 
 

@@ -160,8 +160,7 @@ pkv_status decode_call(void *out, const void *q, const void *key_new, const void
                        const float *k_scales = nullptr, const float *v_scales = nullptr) {
   if (dtype != PKV_BF16) return PKV_ERR_DTYPE;
   const bool fp8 = k_scales != nullptr || v_scales != nullptr;
-  if (fp8 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales) ||
-              key_new != nullptr))
+  if (fp8 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
     return PKV_ERR_ARG;
   if (num_seqs < 0 || num_q_heads < 1 || num_kv_heads < 1 || block_size < 1 || num_blocks < 1 ||
       max_blocks_per_seq < 0 || max_context_len < 0 || !std::isfinite(scale))
@@ -263,6 +262,23 @@ pkv_status pkv_decode_step(void *out, const void *q, const void *key_new, const 
                      v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                      max_context_len, num_q_heads, num_kv_heads, head_dim, block_size,
                      num_blocks, scale, workspace, workspace_bytes, dtype, stream);
+}
+
+pkv_status pkv_decode_step_fp8(void *out, const void *q, const void *key_new,
+                               const void *value_new, int64_t key_token_stride,
+                               int64_t value_token_stride, void *k_cache, void *v_cache,
+                               float *k_scales, float *v_scales, const int32_t *block_tables,
+                               int32_t max_blocks_per_seq, const int32_t *context_lens,
+                               int32_t num_seqs, int32_t max_context_len, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t num_blocks, float scale, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+  if (num_seqs > 0 && (!key_new || !value_new || !k_scales || !v_scales)) return PKV_ERR_ARG;
+  return decode_call(out, q, key_new, value_new, key_token_stride, value_token_stride, k_cache,
+                     v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                     max_context_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                     num_blocks, scale, workspace, workspace_bytes, PKV_BF16, stream, k_scales,
+                     v_scales);
 }
 
 size_t pkv_mixed_workspace_size(int32_t num_decode_seqs, int32_t num_q_heads,

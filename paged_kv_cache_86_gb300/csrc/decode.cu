@@ -112,6 +112,13 @@ struct NewTokens {
   int row_vecs;              // 16-byte vectors per token row (Hkv * 128 bf16)
   int64_t key_stride_vecs;
   int64_t value_stride_vecs;
+  // fp8 E4M3 caches: each (token, KV head) row is quantized on the way in, its
+  // codes to k_cache / v_cache ([slots, Hkv, 128] bytes) and its scale to
+  // k_scales / v_scales ([slots, Hkv])
+  int fp8;
+  int num_kv_heads;
+  float *k_scales;
+  float *v_scales;
 };
 
 __global__ void __launch_bounds__(1024)
@@ -130,7 +137,9 @@ decode_plan_kernel(const int32_t *__restrict__ context_lens, int num_seqs, int m
     // rows spread over many SMs) write its newest token at logical position
     // n - 1, n = context_lens[i] clamped to [0, max_context_len] as below
     // (n = 0 writes nothing): row (n-1) % bs of block block_tables[i][(n-1) / bs].
-    // The decode kernel that reads the cache is the next launch on the stream.
+    // Over fp8 caches each (token, KV head) row is quantized on the way in, as
+    // the fp8 store does it. The decode kernel that reads the cache is the next
+    // launch on the stream.
     const int i = (blockIdx.x - 1) * kStoreSeqsPerCta + (warp >> 2);
     const int part = warp & 3;
     if (i >= num_seqs) return;
@@ -144,6 +153,18 @@ decode_plan_kernel(const int32_t *__restrict__ context_lens, int num_seqs, int m
       return;
     }
     const int64_t row = static_cast<int64_t>(blk) * nt.block_size + pos % nt.block_size;
+    if (nt.fp8) {
+      const uint2 *kin = reinterpret_cast<const uint2 *>(nt.key) + i * nt.key_stride_vecs * 2;
+      const uint2 *vin = reinterpret_cast<const uint2 *>(nt.value) + i * nt.value_stride_vecs * 2;
+      for (int h = part; h < nt.num_kv_heads; h += 4) {
+        const int64_t r8 = row * nt.num_kv_heads + h;
+        const uint2 kb = __ldg(kin + h * 32 + lane);
+        const uint2 vb = __ldg(vin + h * 32 + lane);
+        quantize_row_e4m3(kb, reinterpret_cast<uint32_t *>(nt.k_cache) + r8 * 32, nt.k_scales + r8, lane);
+        quantize_row_e4m3(vb, reinterpret_cast<uint32_t *>(nt.v_cache) + r8 * 32, nt.v_scales + r8, lane);
+      }
+      return;
+    }
     for (int v = part * 32 + lane; v < nt.row_vecs; v += 128) {
       const uint4 kv = __ldg(nt.key + i * nt.key_stride_vecs + v);
       const uint4 vv = __ldg(nt.value + i * nt.value_stride_vecs + v);
@@ -739,6 +760,10 @@ cudaError_t launch_plan(const DecodeArgs &a, int grid, int units_per_token, int 
     nt.row_vecs = a.num_kv_heads * (kHeadDim / 8);
     nt.key_stride_vecs = a.key_stride / 8;
     nt.value_stride_vecs = a.value_stride / 8;
+    nt.fp8 = a.fp8 ? 1 : 0;
+    nt.num_kv_heads = a.num_kv_heads;
+    nt.k_scales = const_cast<float *>(a.k_scales);
+    nt.v_scales = const_cast<float *>(a.v_scales);
     ctas += static_cast<unsigned>((a.num_seqs + kStoreSeqsPerCta - 1) / kStoreSeqsPerCta);
   }
   decode_plan_kernel<<<ctas, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len,

@@ -59,38 +59,8 @@ store_kvcache_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ va
   }
 }
 
-// fp8 E4M3 store: each (token, KV head) row of 128 values is quantized with
-// its own fp32 scale, amax / 448, and codes E4M3(x * (448 / amax)) rounded to
-// nearest even with saturation (cvt.rn.satfinite); a zero row gives zero codes
-// and scale 0 (LLM Infra 101 v0.2, KV Quantization: the cache stores low-bit
-// values instead of bf16). One warp per token; lane l holds dims 4l..4l+3.
-__device__ __forceinline__ uint32_t quantize4_e4m3(uint2 bits, float inv) {
-  const float2 lo = bf16x2_to_float2(bits.x), hi = bf16x2_to_float2(bits.y);
-  uint16_t c01, c23;
-  // cvt packs its first operand into the upper byte
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c01) : "f"(__fmul_rn(lo.y, inv)), "f"(__fmul_rn(lo.x, inv)));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c23) : "f"(__fmul_rn(hi.y, inv)), "f"(__fmul_rn(hi.x, inv)));
-  return static_cast<uint32_t>(c01) | (static_cast<uint32_t>(c23) << 16);
-}
-
-// One 128-element row per warp, four elements per lane (`bits`, already loaded).
-__device__ __forceinline__ void quantize_row_e4m3(const uint2 bits, uint32_t *codes, float *scale,
-                                                  int lane) {
-  const float2 lo = bf16x2_to_float2(bits.x), hi = bf16x2_to_float2(bits.y);
-  float amax = fmaxf(fmaxf(fabsf(lo.x), fabsf(lo.y)), fmaxf(fabsf(hi.x), fabsf(hi.y)));
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  uint32_t c = 0u;
-  float sc = 0.f;
-  if (amax > 0.f) {
-    const float inv = __fdiv_rn(448.f, amax);
-    sc = __fdiv_rn(amax, 448.f);
-    c = quantize4_e4m3(bits, inv);
-  }
-  codes[lane] = c;
-  if (lane == 0) *scale = sc;
-}
-
+// fp8 E4M3 store: one warp per (token, KV head) row; the quantizer
+// (quantize_row_e4m3) is in pkv_device.cuh, shared with the decode step.
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 store_kvcache_fp8_kernel(const __nv_bfloat16 *__restrict__ key,
                          const __nv_bfloat16 *__restrict__ value, uint8_t *__restrict__ k_cache,

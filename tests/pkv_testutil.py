@@ -47,6 +47,23 @@ def compact_inputs(w: Workload, seq_ids, k_cache, v_cache):
     return used, remap, tables, kc.copy(), vc.copy()
 
 
+def per_sequence_rows(w: Workload, t: dict):
+    """New-token rows indexed by sequence, on the device: row i is sequence i's
+    new token (the workload keeps one key/value row per non-empty sequence);
+    zeros for empty ones. The input layout of the fused decode steps."""
+    tok = np.cumsum(w.context_lens > 0) - 1
+    kn = torch.zeros((w.num_seqs, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16,
+                     device=t["key"].device)
+    vn = torch.zeros_like(kn)
+    nz = np.nonzero(w.context_lens > 0)[0]
+    if len(nz):
+        dst = torch.from_numpy(nz).to(kn.device)
+        src = torch.from_numpy(tok[nz]).to(kn.device)
+        kn[dst] = t["key"][src]
+        vn[dst] = t["value"][src]
+    return kn, vn
+
+
 def decode_step_reference(w: Workload, seq_ids, k_cache, v_cache, q, key, value):
     """Oracle store of the chosen sequences' new tokens, then oracle decode.
 

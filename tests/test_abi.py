@@ -120,6 +120,20 @@ def test_fp8_host_validation_needs_no_gpu(lib):
     assert lib.pkv_paged_decode_fp8(null, null, null, null, null, null, null, 4, null, 0, 64, 32,
                                     8, 128, 16, 8, 0.1, null, 0, null) == 0
 
+    # decode step: missing new-token rows or scales, misaligned scales, head_dim,
+    # short stride, no sequences
+    def step(key_new, ks, k_scales, num_seqs=2, head_dim=128):
+        return lib.pkv_decode_step_fp8(a, a, key_new, a, ks, 256, a, a, k_scales, a, a, 4, a,
+                                       num_seqs, 64, 32, 8, head_dim, 16, 8, 0.1, a, 1 << 20, null)
+
+    assert step(null, 256, a) == -1
+    assert step(a, 256, null) == -1
+    assert step(a, 256, vp(260)) == -1
+    assert step(a, 256, a, head_dim=64) == -2
+    assert step(a, 128, a) == -1
+    assert lib.pkv_decode_step_fp8(null, null, null, null, 0, 0, null, null, null, null, null, 4,
+                                   null, 0, 64, 32, 8, 128, 16, 8, 0.1, null, 0, null) == 0
+
 
 def test_mixed_step_host_validation_needs_no_gpu(lib):
     vp, null = ctypes.c_void_p, ctypes.c_void_p(0)

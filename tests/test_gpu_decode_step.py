@@ -10,24 +10,9 @@ import torch
 
 import paged_kv_cache_86_gb300 as pkv
 from paged_kv_cache_86_gb300 import workloads as W
-from pkv_testutil import assert_close, decode_step_reference, device_meta
+from pkv_testutil import assert_close, decode_step_reference, device_meta, per_sequence_rows
 
 pytestmark = pytest.mark.gpu
-
-
-def per_sequence_rows(w, t):
-    """key/value rows indexed by sequence: row i is sequence i's new token
-    (the workload keeps one row per non-empty sequence); zeros for empty ones."""
-    tok = np.cumsum(w.context_lens > 0) - 1
-    kn = torch.zeros((w.num_seqs, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16, device="cuda")
-    vn = torch.zeros_like(kn)
-    nz = np.nonzero(w.context_lens > 0)[0]
-    if len(nz):
-        dst = torch.from_numpy(nz).cuda()
-        src = torch.from_numpy(tok[nz]).cuda()
-        kn[dst] = t["key"][src]
-        vn[dst] = t["value"][src]
-    return kn, vn
 
 
 def run_step(w, t, m):

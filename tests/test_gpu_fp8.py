@@ -1,6 +1,8 @@
 """GPU parity of the fp8 (E4M3, per token-head scale) KV path against the
-oracle: the quantizing store bit for bit (codes and scales), and decode over
-the quantized cache within |gpu - oracle| <= 1e-2 * max(1, |oracle|)."""
+oracle: the quantizing store bit for bit (codes and scales), decode over the
+quantized cache within |gpu - oracle| <= 1e-2 * max(1, |oracle|), and the fused
+fp8 decode step (store of each sequence's newest token + decode in one call)
+against both the oracle and the two separate calls."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +11,7 @@ import paged_kv_cache_86_gb300 as pkv
 from oracle import attention as oracle
 from paged_kv_cache_86_gb300 import workloads as W
 from paged_kv_cache_86_gb300.workloads import bf16_to_u16
-from pkv_testutil import assert_close
+from pkv_testutil import assert_close, per_sequence_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -118,3 +120,57 @@ def test_fp8_decode_late_maximum_rescales_the_accumulator():
     ref, _ = oracle_step_fp8(w, ids, kc, vc, ks, vs, t)
     out = step_fp8(w, t, kc, vc, ks, vs)
     assert_close(out, ref, w.name)
+
+
+def run_step_fp8(w, t, kc, vc, ks, vs):
+    kn, vn = per_sequence_rows(w, t)
+    out = pkv.decode_step_fp8(t["q"], kn, vn, kc, vc, ks, vs,
+                              torch.from_numpy(w.block_tables).cuda(),
+                              torch.from_numpy(w.context_lens).cuda(), w.scale)
+    torch.cuda.synchronize()
+    assert pkv.get_device_errors() == 0
+    return out
+
+
+@pytest.mark.parametrize("hkv,group,bs", [(8, 4, 16), (8, 1, 16), (4, 8, 32), (8, 2, 256)])
+def test_fp8_decode_step_matches_the_oracle(hkv, group, bs):
+    lens = [1, 2, 16, 17, 0, 300, 1023, 5, 129, 2000, 0, 64]
+    w = W.decode_workload(f"fp8_step_{hkv}x{group}_bs{bs}", lens, hkv * group, hkv, bs,
+                          seed=1700 + hkv * 13 + group * 5 + bs)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    kc, vc, ks, vs = fp8_case(w, w.seed)
+    ids = np.arange(w.num_seqs)
+    ref, (k8, v8, k_s, v_s) = oracle_step_fp8(w, ids, kc, vc, ks, vs, t)
+    out = run_step_fp8(w, t, kc, vc, ks, vs)
+    assert np.array_equal(kc.cpu().numpy(), k8) and np.array_equal(vc.cpu().numpy(), v8)
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), k_s.view(np.uint32))
+    assert np.array_equal(vs.cpu().numpy().view(np.uint32), v_s.view(np.uint32))
+    assert_close(out, ref, w.name)
+    for i in np.nonzero(w.context_lens == 0)[0]:
+        assert (out[int(i)] == 0).all()
+
+
+def test_fp8_decode_step_equals_store_then_decode():
+    lens = np.random.default_rng(13).integers(1, 900, size=70)
+    w = W.decode_workload("fp8_step_eq", lens, 32, 8, 16, seed=1313)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    kc, vc, ks, vs = fp8_case(w, w.seed)
+    kc2, vc2, ks2, vs2 = kc.clone(), vc.clone(), ks.clone(), vs.clone()
+    two_calls = step_fp8(w, t, kc2, vc2, ks2, vs2)
+    fused = run_step_fp8(w, t, kc, vc, ks, vs)
+    assert torch.equal(fused, two_calls)
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
+    assert torch.equal(ks.view(torch.int32), ks2.view(torch.int32))
+    assert torch.equal(vs.view(torch.int32), vs2.view(torch.int32))
+
+
+def test_fp8_decode_step_512seq_full_size_sampled():
+    w = W.decode_512seq(fill="device")
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    kc, vc, ks, vs = fp8_case(w, w.seed)
+    rng = np.random.default_rng(16)
+    ids = np.unique(np.concatenate([rng.choice(w.num_seqs, 16, replace=False),
+                                    [int(np.argmax(w.context_lens)), int(np.argmin(w.context_lens))]]))
+    ref, _ = oracle_step_fp8(w, ids, kc, vc, ks, vs, t)
+    out = run_step_fp8(w, t, kc, vc, ks, vs)
+    assert_close(out[torch.from_numpy(ids).cuda()], ref, w.name)
