@@ -39,6 +39,12 @@
 // (480 threads: two converter warpgroups added) the MMA thread polls itself,
 // reading every barrier of a round before issuing that round's MMAs.
 //
+// fp8 caches (E4M3 codes, one scale per token and KV head): the S MMA reads the
+// raw K codes straight from the ring as E4M3 (kind::f8f6f4) against Q^T split
+// into two E4M3 terms whose sum is Q^T (times a power of two per row), and the
+// K scales multiply the scores; V is expanded to f16 by a converter warpgroup
+// and its scales are folded into P, so the PV MMA stays f16.
+//
 // CTA b owns the flat token range [bW, (b+1)W) of the concatenated contexts
 // (all heads), exactly like the split kernel in decode.cu, and leaves the same
 // partial records (o/l, m, l) for sequences a range boundary cuts; decode.cu's
@@ -61,14 +67,12 @@ constexpr int kHD = 128;
 constexpr int kRegion = 16384;        // 128 rows x 128 B (one 64-dim half)
 constexpr int kKVBytes = 2 * kRegion;
 constexpr int kThreads = 256;  // K producer, MMA, 4 softmax warps, V producer, MMA scheduler
-// fp8 caches add two converter warpgroups (warps 7-10: K, 11-14: V); their MMA
+// fp8 caches add two converter warpgroups (warps 7-10: Q, 11-14: V); their MMA
 // warp polls its barriers itself (no scheduler warp)
 constexpr int kThreadsF8 = 480;
 constexpr int kRawCodes = 16384;      // one fp8 stage: 128 rows x 128 one-byte codes
 constexpr int kRawStage = 17408;      // codes + 128 fp32 row scales, padded to 1024 B
-constexpr uint32_t kK0 = 128;         // fp8: first TMEM column of the f16 K stages (64 each)
 constexpr int kMaxN = 128;
-constexpr int kMaxG = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.f;
 constexpr int kSoftmaxBarrier = 1;    // named barrier of the four softmax warps (0 is __syncthreads)
@@ -107,13 +111,13 @@ struct GParams {
 
 // shared-memory map, all offsets from a 1024-aligned base
 struct GLayout {
-  int k, v, q, p, alpha, lsum, msum, desc, bar, vflag, kr, vr, total;
+  int k, v, q, p, alpha, lsum, msum, desc, bar, vflag, qs, kr, vr, total;
 };
 
 __host__ __device__ inline GLayout g_layout(int stages, int n_cols, bool f8 = false) {
   GLayout L;
   const int small = n_cols * 128;         // one 64-dim half of Q^T / P^T (N rows x 128 B)
-  // fp8: the f16 K operand lives in TMEM, so shared memory holds only the V ring
+  // fp8: the S MMA reads the raw K codes, so shared memory holds only the f16 V ring
   L.k = 0;
   L.v = f8 ? 0 : stages * kKVBytes;
   L.q = L.v + stages * kKVBytes;
@@ -125,9 +129,10 @@ __host__ __device__ inline GLayout g_layout(int stages, int n_cols, bool f8 = fa
   L.bar = L.desc + 4 * 32;
   L.vflag = L.bar + 34 * 8 + 16;          // 34 barriers, TMEM slot + abort flag, then V stage flags
   L.total = L.vflag + 16;
-  L.kr = L.vr = 0;
+  L.qs = L.kr = L.vr = 0;
   if (f8) {                               // raw fp8 rings, 1024-aligned for the 128-byte swizzle
-    L.kr = (L.total + 1023) & ~1023;
+    L.qs = L.total;                       // [kMaxN] 1 / scale of each Q^T row (below)
+    L.kr = (L.qs + kMaxN * 4 + 1023) & ~1023;
     L.vr = L.kr + stages * kRawStage;
     L.total = L.vr + stages * kRawStage;
   }
@@ -244,12 +249,104 @@ __device__ __forceinline__ void convert_row_e4m3(uint32_t raw, uint32_t cv, int 
   }
 }
 
-// bf16 -> f16 in place (exact for values of normal f16 magnitude)
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  const float2 f = bf16x2_to_float2(w);
-  uint32_t h;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(f.y), "f"(f.x));  // first operand -> upper half
-  return h;
+// D[tmem] (+)= A[smem desc] * B[smem desc], both E4M3 (kind::f8f6f4; the
+// operand formats come from idesc, 0 = E4M3), f32 accumulator.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Two floats -> two E4M3 codes (round to nearest even, saturating), the first
+// in the low byte; and back, exactly.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(hi), "f"(lo));  // first operand -> upper byte
+  return c;
+}
+
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t codes) {
+  const uint32_t h = e4m3x2_to_f16x2(static_cast<uint16_t>(codes));
+  return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+
+// Q^T for the fp8 S MMA, in place, by 128 threads (t = 0..127; four per row,
+// in one warp): each bf16 row n (dims 0..63 in region 0, 64..127 in region 1,
+// 128-byte rows, 128-byte swizzle) becomes two E4M3 rows hi (region 0) and lo
+// (region 1), 128 codes each, with
+//   q[d] * sq = hi[d] + lo[d],   sq = 2^e, max_d |q[d]| * sq in (224, 448],
+// hi the nearest E4M3 value to q * sq and lo the nearest to what is left. A
+// bf16 value has 8 significant bits and an E4M3 value 4, so hi + lo is q * sq
+// exactly except where lo falls below the E4M3 subnormal step 2^-9 (values
+// under 2^-2 after scaling, about 2^-10 of the row maximum); the error there
+// is at most 2^-10 after scaling. qinv[n] = 1 / sq.
+__device__ __forceinline__ void split_q_e4m3(uint32_t qbuf, uint32_t region, int n_rows, int t,
+                                             float *qinv) {
+  const int quarter = t & 3;                         // dims 32 * quarter .. +31
+  for (int n0 = 0; n0 < n_rows; n0 += 32) {
+    const int n = n0 + (t >> 2);
+    const bool have = n < n_rows;
+    const uint32_t sw = static_cast<uint32_t>(n & 7);
+    uint32_t w[16];                                  // bf16 pairs, dims 32q + 2i, +1
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (have)
+        v = lds128(qbuf + (quarter >> 1) * region + n * 128 +
+                   (((4 * (quarter & 1) + c) ^ sw) << 4));
+      w[4 * c + 0] = v.x;
+      w[4 * c + 1] = v.y;
+      w[4 * c + 2] = v.z;
+      w[4 * c + 3] = v.w;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 f = bf16x2_to_float2(w[i]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    int e = 0;                                       // sq = 2^e
+    if (amax > 0.f && amax <= 3.0e38f) {
+      e = static_cast<int>((__float_as_uint(448.f / amax) >> 23) & 0xffu) - 127;
+      e = max(-126, min(126, e));
+      if (amax * __uint_as_float(static_cast<uint32_t>(e + 127) << 23) > 448.f) --e;
+      e = max(-126, e);
+    }
+    const float sq = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+    __syncwarp();                                    // the row is read before any lane rewrites it
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {                 // code chunk 2q + cc: dims 16 (2q + cc) .. +15
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t hc = 0, lc = 0;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float2 f = bf16x2_to_float2(w[8 * cc + 2 * k + u]);
+          const float x0 = f.x * sq, x1 = f.y * sq;  // exact (power of two)
+          const uint32_t h2 = f32x2_to_e4m3x2(x0, x1);
+          const float2 hv = e4m3x2_to_f32x2(h2);
+          const uint32_t l2 = f32x2_to_e4m3x2(x0 - hv.x, x1 - hv.y);  // the differences are exact
+          hc |= h2 << (16 * u);
+          lc |= l2 << (16 * u);
+        }
+        hi[k] = hc;
+        lo[k] = lc;
+      }
+      if (have) {
+        const uint32_t off = n * 128 + ((static_cast<uint32_t>(2 * quarter + cc) ^ sw) << 4);
+        sts128(qbuf + off, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+        sts128(qbuf + region + off, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+      }
+    }
+    if (have && quarter == 0) qinv[n] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    __syncwarp();
+  }
 }
 
 __device__ __forceinline__ void st_shared_b16(uint32_t addr, float v) {
@@ -493,8 +590,9 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // warps, and a separate scheduler warp measured slower than this thread
     // polling its barriers itself (probes first, then the round's MMAs).
     if (lane == 0) {
-      // fp8 caches: both operands of both MMAs are f16 (A/B format fields 0)
-      constexpr uint32_t kFmt = F8 ? ~((1u << 7) | (1u << 10)) : ~0u;
+      // S is E4M3 x E4M3 (kind::f8f6f4), PV f16 x f16: format field 0 means
+      // E4M3 for the one and f16 for the other
+      constexpr uint32_t kFmt = ~((1u << 7) | (1u << 10));
       const uint32_t idesc_s = umma_idesc_bf16(kRows, N, false) & kFmt;
       const uint32_t idesc_pv = (umma_idesc_bf16(kHD, N, false) | (1u << 15)) & kFmt;  // A (V) MN-major
       bool ok = true;
@@ -536,16 +634,12 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         if (do_s) {
           tc_fence_after();
-          const uint32_t q = sQ;  // one Q^T buffer
+          // S^T = K . (Q_hi + Q_lo)^T: 32 dims per step, the raw K codes
+          // against the hi row (steps 0-3), then against the lo row (4-7)
+          const uint32_t kr = base + L.kr + sj * kRawStage;
 #pragma unroll
-          for (int kk = 0; kk < kHD / 16; ++kk) {
-            if (F8)
-              umma_tmem_a(tmem_s(bj), tmem + kK0 + sj * 64 + kk * 8, desc_k(q, kk, small), idesc_s,
-                          kk > 0 ? 1u : 0u);
-            else
-              umma_bf16(tmem_s(bj), desc_k(sK + sj * kKVBytes, kk, kRegion), desc_k(q, kk, small),
-                        idesc_s, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < 8; ++kk)
+            umma_f8(tmem_s(bj), desc_k(kr, kk & 3, 0), desc_k(sQ, kk, small), idesc_s, kk > 0 ? 1u : 0u);
           umma_commit(s_full(bj));
           first_of = (first_of & ~(1u << (j & 31))) | ((flags & kFirst) ? 1u << (j & 31) : 0u);
           ++s_issued;
@@ -589,9 +683,8 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // issued behind its own MMAs would wait until the tensor core has taken
     // them, so it makes none: it learns each command at a hardware barrier
     // that sums a predicate over the scheduler's lanes.
-    constexpr uint32_t kFmt = F8 ? ~((1u << 7) | (1u << 10)) : ~0u;  // fp8: f16 operands
-    const uint32_t idesc_s = umma_idesc_bf16(kRows, N, false) & kFmt;
-    const uint32_t idesc_pv = (umma_idesc_bf16(kHD, N, false) | (1u << 15)) & kFmt;  // A (V) MN-major
+    const uint32_t idesc_s = umma_idesc_bf16(kRows, N, false);
+    const uint32_t idesc_pv = umma_idesc_bf16(kHD, N, false) | (1u << 15);  // A (V) MN-major
     int s_issued = 0, pv_issued = 0;
     for (;;) {
       const int cmd = bar_red_popc(kIssueBarrier, 64, false);
@@ -612,14 +705,9 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const int j = s_issued, sj = j % S, bj = j & 1;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kHD / 16; ++kk) {
-            if (F8)
-              umma_tmem_a(tmem_s(bj), tmem + kK0 + sj * 64 + kk * 8, desc_k(sQ, kk, small), idesc_s,
-                          kk > 0 ? 1u : 0u);
-            else
-              umma_bf16(tmem_s(bj), desc_k(sK + sj * kKVBytes, kk, kRegion), desc_k(sQ, kk, small),
-                        idesc_s, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kHD / 16; ++kk)
+            umma_bf16(tmem_s(bj), desc_k(sK + sj * kKVBytes, kk, kRegion), desc_k(sQ, kk, small),
+                      idesc_s, kk > 0 ? 1u : 0u);
           umma_commit(s_full(bj));
         }
       }
@@ -706,12 +794,13 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     send(ok ? kCmdFinish : kCmdAbort);
   } else if (F8 && warp >= 7 && warp < 15) {
     // ------------------------------------------------------------ converters
-    // Warps 7-10 expand each raw K stage, warps 11-14 each raw V stage, one
-    // 128-code row per thread, from E4M3 into the f16 operand layout (and, at
-    // a segment's first stage, the new Q^T buffer from bf16 to f16 in place).
+    // Warps 11-14 expand each raw V stage, one 128-code row per thread, from
+    // E4M3 into the f16 operand layout. The S MMA reads the raw K codes as they
+    // landed; warps 7-10 only turn, at a segment's first stage, the new Q^T
+    // buffer into its two E4M3 terms (split_q_e4m3).
     const bool is_k = warp < 11;
-    // K rows go to TMEM, where a warp reaches only its lane quadrant (warp % 4)
-    const int r = is_k ? (warp & 3) * 32 + lane : static_cast<int>(threadIdx.x) - 352;
+    const int r = static_cast<int>(threadIdx.x) - (is_k ? 224 : 352);
+    float *qinv = reinterpret_cast<float *>(smem + L.qs);
     for (int j = 0;; ++j) {
       const int s = j % S;
       if (!warp_wait(is_k ? kr_full(s) : vr_full(s), (j / S) & 1, abort_flag)) {
@@ -724,43 +813,8 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (is_k && lane == 0) mbar_arrive(k_full(s));  // lets the MMA and softmax see the end
         break;
       }
-      if (is_k) {
-        // row r of the raw K stage -> TMEM lane r, columns kK0 + 64 s .. +63 (f16 pairs)
-        const uint32_t raw = base + L.kr + s * kRawStage + r * 128;
-        const uint32_t sw = static_cast<uint32_t>(r & 7);
-        float words[32];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 w = lds128(raw + (((4 * h + c) ^ sw) << 4));
-            const uint4 lo = e4m3x8_to_f16x8(make_uint2(w.x, w.y));
-            const uint4 hi = e4m3x8_to_f16x8(make_uint2(w.z, w.w));
-            words[8 * c + 0] = __uint_as_float(lo.x);
-            words[8 * c + 1] = __uint_as_float(lo.y);
-            words[8 * c + 2] = __uint_as_float(lo.z);
-            words[8 * c + 3] = __uint_as_float(lo.w);
-            words[8 * c + 4] = __uint_as_float(hi.x);
-            words[8 * c + 5] = __uint_as_float(hi.y);
-            words[8 * c + 6] = __uint_as_float(hi.z);
-            words[8 * c + 7] = __uint_as_float(hi.w);
-          }
-          tmem_st32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kK0 + s * 64 + h * 32, words);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-      } else {
-        convert_row_e4m3(base + L.vr + s * kRawStage, sV + s * kKVBytes, r);
-      }
-      if (is_k && (flags & kFirst)) {
-        const uint32_t qbuf = sQ + desc[s].qbuf * 2 * small;
-        for (int i = r; i < static_cast<int>(small) / 8; i += 128) {  // 2 * small bytes, 16 per chunk
-          uint4 w = lds128(qbuf + i * 16);
-          w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
-                         bf16x2_to_f16x2(w.w));
-          sts128(qbuf + i * 16, w);
-        }
-      }
+      if (!is_k) convert_row_e4m3(base + L.vr + s * kRawStage, sV + s * kKVBytes, r);
+      if (is_k && (flags & kFirst)) split_q_e4m3(sQ + desc[s].qbuf * 2 * small, small, N, r, qinv);
       fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
       __syncwarp();
       if (lane == 0) mbar_arrive(is_k ? k_full(s) : v_full(s));
@@ -784,6 +838,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     int segs_done = 0;
     bool ok = true;
+    // fp8: 1 / scale of the Q^T rows of this row's query heads (S^T column
+    // h*G + g), set at each segment's first stage
+    float qinv[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) qinv[g] = 1.f;
     // P^T (N rows x 128 stage rows, K-major, 128-byte swizzle): element (n, r)
     const uint32_t p_half = (r >> 6) * small;
     const int rc = r & 63;
@@ -804,8 +863,13 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         d = desc[s];
         // fp8: this row's K scale sits in the raw stage, which the loader may
         // refill once every softmax warp has arrived on k_empty (below)
-        if (F8 && !(d.flags & kEnd))
+        if (F8 && !(d.flags & kEnd)) {
           kscale = reinterpret_cast<const float *>(smem + L.kr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
+          if (d.flags & kFirst) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) qinv[g] = reinterpret_cast<const float *>(smem + L.qs)[head * G + g];
+          }
+        }
       }
       const bool end = ok && (d.flags & kEnd);
       const bool work = ok && !end;
@@ -836,7 +900,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           float v = cols[g];
 #pragma unroll
           for (int k = 1; k < kHeadsInWarp; ++k) v = (my_slot == k) ? cols[k * G + g] : v;
-          sc[g] = valid ? v * (F8 ? p.scale_log2 * kscale : p.scale_log2) : -INFINITY;
+          sc[g] = valid ? v * (F8 ? p.scale_log2 * kscale * qinv[g] : p.scale_log2) : -INFINITY;
         }
         if (first) {
           // a segment's first stage fixes the reference maximum of each query
@@ -1122,10 +1186,6 @@ cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *
   if (!maps_ok) return cudaErrorInvalidValue;
   int tmem_cols = 32;
   while (tmem_cols < 3 * n_cols + 16) tmem_cols <<= 1;
-  if (f8) {  // O^T and S^T below column kK0, then the f16 K stages
-    if (3 * n_cols + 16 > static_cast<int>(kK0)) return cudaErrorInvalidValue;
-    tmem_cols = 512;
-  }
   GParams p;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.block_tables = a.block_tables;
