@@ -174,3 +174,22 @@ def test_fp8_decode_step_512seq_full_size_sampled():
     ref, _ = oracle_step_fp8(w, ids, kc, vc, ks, vs, t)
     out = run_step_fp8(w, t, kc, vc, ks, vs)
     assert_close(out[torch.from_numpy(ids).cuda()], ref, w.name)
+
+
+def test_fp8_decode_extreme_query_magnitudes():
+    # per query head the kernel scales Q by a power of two before splitting it
+    # into two E4M3 terms: rows far above the E4M3 range (448) and far below
+    # its normal range must come out as with a plain Q
+    hkv, group, bs = 8, 4, 16
+    lens = [300, 2000, 700, 64, 17, 1]
+    w = W.decode_workload("fp8_q_range", lens, hkv * group, hkv, bs, seed=4242)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    big = torch.tensor([3.0e4, 1.0, 1.0e-4, 5.0e3, 1.0, 2.0e-5], device="cuda")
+    t["q"] = (t["q"].float() * big[:, None, None] / 128 ** 0.5 * 0.05).to(torch.bfloat16)
+    t["q"][1, 5] *= 1.0e4          # one head of an ordinary row far above the rest
+    kc, vc, ks, vs = fp8_case(w, w.seed)
+    ids = np.arange(w.num_seqs)
+    ref, _ = oracle_step_fp8(w, ids, kc, vc, ks, vs, t)
+    out = step_fp8(w, t, kc, vc, ks, vs)
+    assert torch.isfinite(out.float()).all()
+    assert_close(out, ref, w.name)
