@@ -193,3 +193,69 @@ def test_fp8_decode_extreme_query_magnitudes():
     out = step_fp8(w, t, kc, vc, ks, vs)
     assert torch.isfinite(out.float()).all()
     assert_close(out, ref, w.name)
+
+
+def test_fp8_decode_step_replays_from_a_cuda_graph_at_a_padded_batch():
+    """29 live sequences padded to a captured batch of 48 with empty rows; the
+    fp8 step is replayed for three consecutive steps (context_lens grows by one
+    and new q / K / V rows arrive each step, all through the same buffers)."""
+    live, padded, hkv, group, bs = 29, 48, 8, 4, 16
+    rng = np.random.default_rng(19)
+    lens0 = (rng.integers(0, 30, size=live) * bs + rng.integers(1, bs - 3, size=live)).astype(np.int32)
+    grown = np.concatenate([lens0 + 3, np.zeros(padded - live, np.int32)])  # blocks for 3 steps
+    w0 = W.decode_workload("graph_pad_fp8", grown, hkv * group, hkv, bs, seed=78)
+    kc, vc, ks, vs = fp8_case(w0, w0.seed)
+    bt = torch.from_numpy(w0.block_tables).cuda()
+    cl = torch.zeros(padded, dtype=torch.int32, device="cuda")
+    q = torch.zeros((padded, hkv * group, 128), dtype=torch.bfloat16, device="cuda")
+    kn = torch.zeros((padded, hkv, 128), dtype=torch.bfloat16, device="cuda")
+    vn = torch.zeros_like(kn)
+    out = torch.empty_like(q)
+    ws = torch.empty(pkv.decode_workspace_size(padded, hkv * group, hkv), dtype=torch.uint8,
+                     device="cuda")
+    max_ctx = int(w0.block_tables.shape[1] * bs)
+
+    def step():
+        pkv.decode_step_fp8(q, kn, vn, kc, vc, ks, vs, bt, cl, w0.scale, max_context_len=max_ctx,
+                            out=out, workspace=ws)
+
+    step()  # eager call first: one-time function attributes are set outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+
+    gen = torch.Generator(device="cuda").manual_seed(6)
+    mask = np.zeros(padded, np.uint8)
+    mask[:live] = 1
+    for k in range(3):
+        lens = np.concatenate([lens0 + k, np.zeros(padded - live, np.int32)]).astype(np.int32)
+        cl.copy_(torch.from_numpy(lens))
+        q.normal_(generator=gen)
+        kn.normal_(generator=gen)
+        vn.normal_(generator=gen)
+        q[live:] = 0
+        kn[live:] = 0
+        vn[live:] = 0
+        # the oracle's view of this step: host copies of the pool before the replay
+        k8, v8 = kc.cpu().numpy().copy(), vc.cpu().numpy().copy()
+        k_s, v_s = ks.cpu().numpy().copy(), vs.cpu().numpy().copy()
+        slots = np.array([w0.block_tables[i, (n - 1) // bs] * bs + (n - 1) % bs
+                          for i, n in enumerate(lens[:live])], dtype=np.int32)
+        oracle.store_kvcache_fp8(bf16_to_u16(kn[:live]), bf16_to_u16(vn[:live]), k8, v8, k_s, v_s,
+                                 slots, bs)
+        ref = oracle.paged_decode_fp8(bf16_to_u16(q), k8, v8, k_s, v_s, w0.block_tables, lens,
+                                      w0.scale, seq_mask=mask)[:live]
+        g.replay()
+        torch.cuda.synchronize()
+        assert pkv.get_device_errors() == 0
+        assert np.array_equal(kc.cpu().numpy(), k8) and np.array_equal(vc.cpu().numpy(), v8)
+        assert np.array_equal(ks.cpu().numpy().view(np.uint32), k_s.view(np.uint32))
+        assert np.array_equal(vs.cpu().numpy().view(np.uint32), v_s.view(np.uint32))
+        assert_close(out[:live], ref, f"fp8 graph step {k}")
+        assert (out[live:] == 0).all()
