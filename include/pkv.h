@@ -171,9 +171,13 @@ pkv_status pkv_store_kvcache_fp8(const void *key, const void *value,
 
 /* pkv_paged_decode_fp8: pkv_paged_decode over fp8 caches -- the attention of
  * each q row over the dequantized K/V rows. Same arguments, workspace and
- * errors as pkv_paged_decode, plus the scale arrays. q and out stay bf16; q
- * enters the tensor core as f16 (exact for |q| in the normal f16 range, up to
- * 65504). Supported: head_dim 128, num_kv_heads 4 or 8, num_q_heads /
+ * errors as pkv_paged_decode, plus the scale arrays. q and out stay bf16. The
+ * K codes enter the tensor core as E4M3, against each q row scaled by a power
+ * of two and split into two E4M3 terms whose sum is the scaled row (exact for
+ * bf16 q except for entries under about 2^-10 of the row's largest, off by at
+ * most 2^-10 of the scaled unit there); V is expanded to f16 with its row
+ * scales folded into the softmax weights. Supported: head_dim 128,
+ * num_kv_heads 4 or 8, num_q_heads /
  * num_kv_heads in {1, 2, 4, 8} with num_q_heads <= 32, block_size a multiple
  * of 128 / num_kv_heads; other shapes return PKV_ERR_SHAPE.
  */

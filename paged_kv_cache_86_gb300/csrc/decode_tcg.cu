@@ -356,7 +356,8 @@ __device__ __forceinline__ void st_shared_b16(uint32_t addr, float v) {
 }
 
 // T: tokens per stage (128 / Hkv); G: query heads per KV head; F8: the caches
-// hold E4M3 codes with per-row scales (operands converted to f16 on chip).
+// hold E4M3 codes with per-row scales (K read by the MMA as E4M3, V expanded
+// to f16 on chip).
 template <int T, int G, bool F8>
 __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
 decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
