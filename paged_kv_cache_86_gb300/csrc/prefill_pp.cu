@@ -100,6 +100,12 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_base, int kk) {
   return smem_desc_sw128(tile_base + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024);
 }
 
+// start-address increment (16-byte units, the descriptor's low field) of K
+// step kk from step 0 of a K-major tile
+__device__ __forceinline__ uint64_t kmajor_step(int kk) {
+  return static_cast<uint64_t>(((kk >> 2) * kRegion + (kk & 3) * 32) >> 4);
+}
+
 __device__ __forceinline__ uint64_t desc_v_mnmajor(uint32_t tile_base, int kk) {
   return smem_desc_sw128(tile_base + kk * 2048, kRegion, 1024);
 }
@@ -373,10 +379,11 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         int kbase = 0, vbase = 0, items = 0;
         auto issue_s = [&](int x, int kt, bool last_s) {
           const int s = kt % kKStages;
-          const uint32_t q = sQ + x * kTileBytes;
+          // descriptors of step 0; later steps only move the start address
+          const uint64_t dq = desc_kmajor(sQ + x * kTileBytes, 0), dk = desc_kmajor(sK(s), 0);
 #pragma unroll
           for (int kk = 0; kk < kHD / 16; ++kk)
-            umma_bf16(tmem_s(x), desc_kmajor(q, kk), desc_kmajor(sK(s), kk), idesc_s, kk > 0 ? 1u : 0u);
+            umma_bf16(tmem_s(x), dq + kmajor_step(kk), dk + kmajor_step(kk), idesc_s, kk > 0 ? 1u : 0u);
           umma_commit(s_full(x));
           ++s_commits[x];
           if (x == 1) {
@@ -391,9 +398,10 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           // must have read it out
           if (j == 0 && items > 0 && !mbar_wait(o_free(x), (items - 1) & 1, abort_flag)) return false;
           tc_fence_after();
+          const uint64_t dv = desc_v_mnmajor(sV(s), 0);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_bf16_tmem_a(tmem_o(x), tmem_s(x) + kk * 8, desc_v_mnmajor(sV(s), kk), idesc_pv,
+            umma_bf16_tmem_a(tmem_o(x), tmem_s(x) + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc_pv,
                              (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(pv_done(x));
           ++pv_commits[x];
