@@ -198,6 +198,13 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk, uint32_t regio
   return smem_desc_sw128(base + (kk >> 2) * region + (kk & 3) * 32, 16, 1024);
 }
 
+// start-address increment (16-byte units, the descriptor's low field) of K
+// step kk from step 0 of a K-major operand with 64-dim regions region16 * 16
+// bytes apart: the issuing thread builds a descriptor once per group and steps it
+__device__ __forceinline__ uint64_t kstep(int kk, uint32_t region16) {
+  return static_cast<uint64_t>((kk >> 2) * region16 + (kk & 3) * 2);
+}
+
 __device__ __forceinline__ uint64_t desc_v(uint32_t base, int kk) {
   return smem_desc_sw128(base + kk * 2048, kRegion, 1024);
 }
@@ -637,10 +644,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           tc_fence_after();
           // S^T = K . (Q_hi + Q_lo)^T: 32 dims per step, the raw K codes
           // against the hi row (steps 0-3), then against the lo row (4-7)
-          const uint32_t kr = base + L.kr + sj * kRawStage;
+          const uint64_t dkr = desc_k(base + L.kr + sj * kRawStage, 0, 0), dq = desc_k(sQ, 0, small);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_f8(tmem_s(bj), desc_k(kr, kk & 3, 0), desc_k(sQ, kk, small), idesc_s, kk > 0 ? 1u : 0u);
+            umma_f8(tmem_s(bj), dkr + kstep(kk & 3, 0), dq + kstep(kk, small >> 4), idesc_s, kk > 0 ? 1u : 0u);
           umma_commit(s_full(bj));
           first_of = (first_of & ~(1u << (j & 31))) | ((flags & kFirst) ? 1u << (j & 31) : 0u);
           ++s_issued;
@@ -649,9 +656,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (do_pv) {
           tc_fence_after();
           const bool first = (first_of >> (t & 31)) & 1u;
+          const uint64_t dv = desc_v(sV + st * kKVBytes, 0), dp = desc_k(sP + (t & 1) * 2 * small, 0, small);
 #pragma unroll
           for (int kk = 0; kk < kRows / 16; ++kk)
-            umma_bf16(tmem_o, desc_v(sV + st * kKVBytes, kk), desc_k(sP + (t & 1) * 2 * small, kk, small),
+            umma_bf16(tmem_o, dv + static_cast<uint64_t>(kk * (2048 >> 4)), dp + kstep(kk, small >> 4),
                       idesc_pv, (first && kk == 0) ? 0u : 1u);
           umma_commit(pv_done(t & 1));
           umma_commit(v_empty(st));
@@ -695,9 +703,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const int t = pv_issued, st = t % S;
           const bool first = (cmd & kCmdPVFirst) != 0;
           tc_fence_after();
+          const uint64_t dv = desc_v(sV + st * kKVBytes, 0), dp = desc_k(sP + (t & 1) * 2 * small, 0, small);
 #pragma unroll
           for (int kk = 0; kk < kRows / 16; ++kk)
-            umma_bf16(tmem_o, desc_v(sV + st * kKVBytes, kk), desc_k(sP + (t & 1) * 2 * small, kk, small),
+            umma_bf16(tmem_o, dv + static_cast<uint64_t>(kk * (2048 >> 4)), dp + kstep(kk, small >> 4),
                       idesc_pv, (first && kk == 0) ? 0u : 1u);
           umma_commit(pv_done(t & 1));
           umma_commit(v_empty(st));
@@ -705,10 +714,11 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (cmd & kCmdS) {
           const int j = s_issued, sj = j % S, bj = j & 1;
           tc_fence_after();
+          const uint64_t dk = desc_k(sK + sj * kKVBytes, 0, kRegion), dq = desc_k(sQ, 0, small);
 #pragma unroll
           for (int kk = 0; kk < kHD / 16; ++kk)
-            umma_bf16(tmem_s(bj), desc_k(sK + sj * kKVBytes, kk, kRegion), desc_k(sQ, kk, small),
-                      idesc_s, kk > 0 ? 1u : 0u);
+            umma_bf16(tmem_s(bj), dk + kstep(kk, kRegion >> 4), dq + kstep(kk, small >> 4), idesc_s,
+                      kk > 0 ? 1u : 0u);
           umma_commit(s_full(bj));
         }
       }

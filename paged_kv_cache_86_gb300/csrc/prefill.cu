@@ -91,6 +91,13 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_base, int kk) {
   return smem_desc_sw128(tile_base + (kk >> 2) * kRegion + (kk & 3) * 32, 16, 1024);
 }
 
+// start-address increment (16-byte units, the descriptor's low field) of K
+// step kk from step 0 of a K-major tile: the issuing thread builds each
+// descriptor once per group and steps it
+__device__ __forceinline__ uint64_t kmajor_step(int kk) {
+  return static_cast<uint64_t>(((kk >> 2) * kRegion + (kk & 3) * 32) >> 4);
+}
+
 __device__ __forceinline__ uint64_t desc_v_mnmajor(uint32_t tile_base, int kk) {
   // 16 keys = two 8-row groups (1024 bytes each); N = 128 dims = two regions
   return smem_desc_sw128(tile_base + kk * 2048, kRegion, 1024);
@@ -253,9 +260,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!mbar_wait(v_full(s), (t / kStages) & 1, abort_flag)) return false;
         if (!mbar_wait(p_full, t & 1, abort_flag)) return false;
         tc_fence_after();
+        const uint64_t dp = desc_kmajor(sP, 0), dv = desc_v_mnmajor(sV(s), 0);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16(tmem_o, desc_kmajor(sP, kk), desc_v_mnmajor(sV(s), kk), idesc_pv,
+          umma_bf16(tmem_o, dp + kmajor_step(kk), dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc_pv,
                     (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(pv_done);
         umma_commit(v_empty(s));
@@ -268,9 +276,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (ok && j > 0) ok = mbar_wait(s_free, (j - 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
+        const uint64_t dq = desc_kmajor(sQ, 0), dk = desc_kmajor(sK(s), 0);
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk)
-          umma_bf16(tmem_s, desc_kmajor(sQ, kk), desc_kmajor(sK(s), kk), idesc_s, kk > 0 ? 1u : 0u);
+          umma_bf16(tmem_s, dq + kmajor_step(kk), dk + kmajor_step(kk), idesc_s, kk > 0 ? 1u : 0u);
         umma_commit(s_full);
         umma_commit(k_empty(s));
         ++s_issued;
