@@ -102,8 +102,15 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_base, int kk) {
 
 // start-address increment (16-byte units, the descriptor's low field) of K
 // step kk from step 0 of a K-major tile
-__device__ __forceinline__ uint64_t kmajor_step(int kk) {
-  return static_cast<uint64_t>(((kk >> 2) * kRegion + (kk & 3) * 32) >> 4);
+__device__ __forceinline__ uint32_t kmajor_step(int kk) {
+  return static_cast<uint32_t>(((kk >> 2) * kRegion + (kk & 3) * 32) >> 4);
+}
+
+// descriptor d with its start address moved by `step` 16-byte units: a 32-bit
+// add, since the 14-bit address field (shared memory is under 256 KB) never
+// carries into the descriptor's upper word
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t step) {
+  return (d & 0xFFFFFFFF00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(d) + step);
 }
 
 __device__ __forceinline__ uint64_t desc_v_mnmajor(uint32_t tile_base, int kk) {
@@ -383,7 +390,8 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const uint64_t dq = desc_kmajor(sQ + x * kTileBytes, 0), dk = desc_kmajor(sK(s), 0);
 #pragma unroll
           for (int kk = 0; kk < kHD / 16; ++kk)
-            umma_bf16(tmem_s(x), dq + kmajor_step(kk), dk + kmajor_step(kk), idesc_s, kk > 0 ? 1u : 0u);
+            umma_bf16(tmem_s(x), desc_at(dq, kmajor_step(kk)), desc_at(dk, kmajor_step(kk)), idesc_s,
+                      kk > 0 ? 1u : 0u);
           umma_commit(s_full(x));
           ++s_commits[x];
           if (x == 1) {
@@ -401,7 +409,7 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const uint64_t dv = desc_v_mnmajor(sV(s), 0);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_bf16_tmem_a(tmem_o(x), tmem_s(x) + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc_pv,
+            umma_bf16_tmem_a(tmem_o(x), tmem_s(x) + kk * 8, desc_at(dv, kk * (2048 >> 4)), idesc_pv,
                              (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(pv_done(x));
           ++pv_commits[x];
