@@ -7,8 +7,10 @@
 // same compute-bound regime (Mini-SGLang 源码解析（二）§8.3). What changes is
 // the schedule, so that the tensor core never waits for a softmax:
 //
-//   * One CTA = one 128-row query tile of TWO query heads A and B of the same
-//     KV head (GQA): the K and V tiles are loaded once for both.
+//   * One work item = one 128-row query tile of TWO query heads A and B of the
+//     same KV head (GQA), or, when the GQA group is odd, two consecutive query
+//     tiles A and B of one head: either way the K and V tiles are loaded once
+//     for both.
 //   * Two softmax warpgroups (warps 0-3 for A, 4-7 for B). While one computes
 //     the softmax of its tile, the tensor core runs the other head's S and PV.
 //     The third warpgroup holds the Q/K loader (warp 8), the MMA issuer (warp
@@ -85,6 +87,7 @@ struct PPParams {
   int causal;
   int box_rows;
   int q_tiles;       // 128-row query tiles of the longest chunk
+  int pair_tiles;    // odd GQA group: A and B are two consecutive query tiles of one head
   uint32_t *ticket;  // next unclaimed work item (zeroed before the launch)
   float scale_log2;
   uint32_t *err;
@@ -160,14 +163,22 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // is query tile (last first) w % n_xt of head pair (w / n_xt) % n_hp of
   // sequence w / (n_xt * n_hp): items claimed close in time read the K/V of a
   // few sequences (L2 reuse). All roles walk the same items, skip the same ones.
-  const int n_xt = p.q_tiles, n_hp = p.num_q_heads / 2;
+  // With an odd GQA group the two heads of a pair would read different K/V, so
+  // A and B are instead two consecutive query tiles of one head (a "tile" of
+  // the walk is then 256 rows): they still share every K/V tile, and A's rows
+  // mask the last one, which only B needs.
+  const int xt_rows = p.pair_tiles ? 2 * kTile : kTile;   // rows of the walk's tile
+  const int n_xt = p.pair_tiles ? (p.q_tiles + 1) / 2 : p.q_tiles;
+  const int n_hp = p.pair_tiles ? p.num_q_heads : p.num_q_heads / 2;
+  const int head_step = p.pair_tiles ? 0 : 1;             // head of B = head of A + head_step
+  const int row_step = p.pair_tiles ? kTile : 0;          // first row of B = first row of A + row_step
   const int n_items = n_xt * n_hp * p.num_seqs;
   struct Item {
     int seq, qh_a, r0, q_begin, q_len, k_len, prefix, n_tiles, kvh;
   };
   auto item_at = [&](int w, Item &it) -> bool {
-    it.r0 = (n_xt - 1 - w % n_xt) * kTile;
-    it.qh_a = 2 * ((w / n_xt) % n_hp);
+    it.r0 = (n_xt - 1 - w % n_xt) * xt_rows;
+    it.qh_a = (1 + head_step) * ((w / n_xt) % n_hp);
     it.seq = w / (n_xt * n_hp);
     it.q_begin = p.cu_q[it.seq];
     const int q_end = p.cu_q[it.seq + 1];
@@ -180,7 +191,7 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     if (it.r0 >= it.q_len) return false;
     it.prefix = p.causal ? it.k_len - it.q_len : 0;
-    const int last_row = min(it.r0 + kTile - 1, it.q_len - 1);
+    const int last_row = min(it.r0 + xt_rows - 1, it.q_len - 1);
     const int key_end = p.causal ? min(it.prefix + last_row + 1, it.k_len) : it.k_len;
     it.n_tiles = (key_end + kTile - 1) / kTile;
     it.kvh = it.qh_a / p.group;
@@ -321,8 +332,10 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             } else {
               mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
               for (int x = 0; x < 2; ++x) {
-                tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, it.qh_a + x, it.q_begin + it.r0, q_full);
-                tma_load_3d(sQ + x * kTileBytes + kRegion, &tm_q, 64, it.qh_a + x, it.q_begin + it.r0,
+                tma_load_3d(sQ + x * kTileBytes, &tm_q, 0, it.qh_a + x * head_step,
+                            it.q_begin + it.r0 + x * row_step, q_full);
+                tma_load_3d(sQ + x * kTileBytes + kRegion, &tm_q, 64, it.qh_a + x * head_step,
+                            it.q_begin + it.r0 + x * row_step,
                             q_full);
               }
             }
@@ -480,7 +493,8 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       if (w >= n_items) break;
       if (!item_at(w, it)) continue;
-      const int qpos = it.prefix + it.r0 + r;
+      const int r0x = it.r0 + x * row_step;            // first row of this warpgroup's tile
+      const int qpos = it.prefix + r0x + r;
       const int visible = p.causal ? min(qpos + 1, it.k_len) : it.k_len;
       float m_used = -INFINITY, l_sum = 0.f;         // running max of raw scores, row sum
 
@@ -556,9 +570,9 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ok = warp_wait(pv_done(x), (tiles_done + it.n_tiles - 1) & 1, abort_flag);
         tc_fence_after();
       }
-      const bool store = (it.r0 + r) < it.q_len;
-      __nv_bfloat16 *orow = p.out + (static_cast<size_t>(it.q_begin) + it.r0 + r) * p.num_q_heads * kHD +
-                            static_cast<size_t>(it.qh_a + x) * kHD;
+      const bool store = (r0x + r) < it.q_len;
+      __nv_bfloat16 *orow = p.out + (static_cast<size_t>(it.q_begin) + r0x + r) * p.num_q_heads * kHD +
+                            static_cast<size_t>(it.qh_a + x * head_step) * kHD;
       const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
@@ -634,8 +648,7 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t heads,
 }  // namespace
 
 bool prefill_pp_supported(int num_q_heads, int num_kv_heads, int block_size) {
-  return num_kv_heads >= 1 && num_q_heads % num_kv_heads == 0 &&
-         (num_q_heads / num_kv_heads) % 2 == 0 && block_size % 8 == 0;
+  return num_kv_heads >= 1 && num_q_heads % num_kv_heads == 0 && block_size % 8 == 0;
 }
 
 cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
@@ -679,11 +692,14 @@ cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
   p.scale_log2 = a.scale * kLog2e;
   p.err = a.err;
   p.q_tiles = (a.max_seqlen_q + kTile - 1) / kTile;
+  p.pair_tiles = (p.group % 2 != 0) ? 1 : 0;
   p.ticket = static_cast<uint32_t *>(a.workspace);
   if (p.ticket == nullptr) return cudaErrorInvalidValue;
   if (!a.ticket_zeroed)
     if (cudaError_t me = cudaMemsetAsync(p.ticket, 0, sizeof(uint32_t), stream)) return me;
-  const long long n_items = static_cast<long long>(p.q_tiles) * (a.num_q_heads / 2) * a.num_seqs;
+  const long long n_items =
+      p.pair_tiles ? static_cast<long long>((p.q_tiles + 1) / 2) * a.num_q_heads * a.num_seqs
+                   : static_cast<long long>(p.q_tiles) * (a.num_q_heads / 2) * a.num_seqs;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

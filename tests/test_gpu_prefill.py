@@ -56,6 +56,14 @@ def test_prefill_block_sizes(bs):
     check(W.prefill_workload(f"p_bs{bs}", [130, 77], [300, 45], 16, 8, bs, seed=300 + bs))
 
 
+@pytest.mark.parametrize("hkv,group", [(3, 3), (2, 5), (4, 1), (1, 3)])
+def test_prefill_odd_groups_pair_query_tiles(hkv, group):
+    # odd GQA groups run two consecutive 128-row query tiles of one head per
+    # work item: ragged pairs (300 = 256 + 44 rows, 257, 33) and a full one (512)
+    check(W.prefill_workload(f"p_odd_h{hkv}g{group}", [300, 512, 33, 257], [100, 0, 700, 31],
+                             hkv * group, hkv, 16, seed=500 + hkv * 10 + group))
+
+
 @pytest.mark.parametrize("hkv,group", [(8, 1), (4, 2), (8, 4), (2, 8), (1, 4)])
 def test_prefill_head_groups(hkv, group):
     check(W.prefill_workload(f"p_h{hkv}g{group}", [140, 33], [200, 7], hkv * group, hkv, 16,
