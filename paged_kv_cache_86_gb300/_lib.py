@@ -111,6 +111,17 @@ def _need(t: torch.Tensor, name: str, dtype, ndim=None):
         raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
 
 
+def _out_like(out, q: torch.Tensor) -> torch.Tensor:
+    """The caller's output buffer (checked: bf16, contiguous, shaped like q, on q's
+    device), or a new one."""
+    if out is None:
+        return torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, q.dim())
+    if out.shape != q.shape or not out.is_contiguous() or out.device != q.device:
+        raise ValueError("out must be a contiguous tensor shaped like q, on q's device")
+    return out
+
+
 def _ptr(t: torch.Tensor):
     return ctypes.c_void_p(t.data_ptr())
 
@@ -197,8 +208,7 @@ def paged_decode_fp8(q, k_cache, v_cache, k_scales, v_scales, block_tables, cont
     mb = block_tables.shape[1]
     if max_context_len is None:
         max_context_len = mb * bs
-    if out is None:
-        out = torch.empty_like(q)
+    out = _out_like(out, q)
     need = decode_workspace_size(s, hq, hkv, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
@@ -239,11 +249,7 @@ def decode_step_fp8(q, key_new, value_new, k_cache, v_cache, k_scales, v_scales,
     mb = block_tables.shape[1]
     if max_context_len is None:
         max_context_len = mb * bs
-    if out is None:
-        out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, 3)
-    if out.shape != q.shape or not out.is_contiguous():
-        raise ValueError("out must be a contiguous tensor shaped like q")
+    out = _out_like(out, q)
     need = decode_workspace_size(s, hq, hkv, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
@@ -289,8 +295,7 @@ def mixed_step(q, key, value, slot_mapping, k_cache, v_cache, cu_seqlens_q, cu_s
             or slot_mapping.shape[0] != total_q or key.shape != (total_q, hkv, d)
             or value.shape != (total_q, hkv, d)):
         raise ValueError("metadata shape mismatch")
-    if out is None:
-        out = torch.empty_like(q)
+    out = _out_like(out, q)
     need = mixed_workspace_size(num_decode_seqs, hq, hkv, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
@@ -364,11 +369,7 @@ def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float,
     mb = block_tables.shape[1]
     if max_context_len is None:
         max_context_len = mb * bs
-    if out is None:
-        out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, 3)
-    if out.shape != q.shape or not out.is_contiguous():
-        raise ValueError("out must be a contiguous tensor shaped like q")
+    out = _out_like(out, q)
     need = decode_workspace_size(s, hq, hkv, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
@@ -410,11 +411,7 @@ def decode_step(q, key_new, value_new, k_cache, v_cache, block_tables, context_l
     mb = block_tables.shape[1]
     if max_context_len is None:
         max_context_len = mb * bs
-    if out is None:
-        out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, 3)
-    if out.shape != q.shape or not out.is_contiguous():
-        raise ValueError("out must be a contiguous tensor shaped like q")
+    out = _out_like(out, q)
     need = decode_workspace_size(s, hq, hkv, d)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
@@ -448,8 +445,7 @@ def paged_prefill(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables,
     s = cu_seqlens_q.shape[0] - 1
     if cu_seqlens_k.shape[0] != s + 1 or block_tables.shape[0] != s:
         raise ValueError("metadata shape mismatch")
-    if out is None:
-        out = torch.empty_like(q)
+    out = _out_like(out, q)
     need = prefill_workspace_size(s, total_q, hq, d)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
