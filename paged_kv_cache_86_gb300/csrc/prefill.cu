@@ -22,12 +22,12 @@
 namespace pkv {
 
 bool prefill_supported(int num_q_heads, int num_kv_heads, int block_size) {
-  return num_kv_heads >= 1 && num_q_heads % num_kv_heads == 0 && block_size % 8 == 0;
+  return prefill_pp_supported(num_q_heads, num_kv_heads, block_size);
 }
 
 cudaError_t launch_paged_prefill(const PrefillArgs &a, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.total_q == 0 || a.max_seqlen_q == 0) return cudaSuccess;
-  if (!prefill_pp_supported(a.num_q_heads, a.num_kv_heads, a.block_size)) return cudaErrorInvalidValue;
+  if (!prefill_supported(a.num_q_heads, a.num_kv_heads, a.block_size)) return cudaErrorInvalidValue;
   return launch_prefill_pp(a, stream);
 }
 
