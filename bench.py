@@ -214,13 +214,17 @@ def profiled_traffic(name):
 
 # ------------------------------------------------------------ cpu oracle --
 
-def cpu_oracle_sample(w, target_s=15.0, max_seqs=None):
+def cpu_oracle_sample(w, target_s=15.0, max_seqs=None, threads=None):
     """Time the oracle (store of the new tokens + decode) on a bounded sample of
-    the workload's sequences, on this host's cores. Returns a cpu_baseline dict."""
+    the workload's sequences, on this host's cores (or on `threads` of them).
+    Returns a cpu_baseline dict."""
     import torch
     from oracle import attention as oracle
     from paged_kv_cache_86_gb300.workloads import bf16_to_u16
 
+    prev_threads = oracle.max_threads()
+    if threads:
+        oracle.set_threads(threads)
     cores = oracle.max_threads()
     order = np.random.default_rng(0).permutation(w.num_seqs)
     t = w.tensors
@@ -257,11 +261,13 @@ def cpu_oracle_sample(w, target_s=15.0, max_seqs=None):
         elapsed += time.perf_counter() - t0
         done_seqs += len(ids)
         done_tokens += int(lens.sum())
+    if threads:
+        oracle.set_threads(prev_threads)
     value = done_seqs / elapsed if elapsed > 0 else None
     return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{done_seqs} sequences of the {w.num_seqs}-sequence batch in seeded random "
                       f"order, cycling ({done_tokens} cached tokens), store + decode in fp64 C "
-                      f"with OpenMP, {elapsed:.1f} s",
+                      f"with OpenMP on {cores} thread(s), {elapsed:.1f} s",
             "seconds": elapsed}
 
 
@@ -433,6 +439,8 @@ def run_pkv(args, rank, world, device):
     result["mixed_batch_row"] = measure_mixed(device, steps=max(5, min(args.steps, 20)))
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_oracle_sample(w)
+        one = cpu_oracle_sample(w, target_s=5.0, threads=1)   # the same oracle on one core
+        result["cpu_baseline"]["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
     return result
 
 
