@@ -57,9 +57,14 @@ def parse():
                     help="warm-up and timed steps only: no per-op, e2e, clocks or CPU legs")
     ap.add_argument("--only-prefill", action="store_true",
                     help="time only the chunked-prefill row (store + prefill), for profiling")
-    ap.add_argument("--only-row", choices=["fp8", "copy", "mixed"], default=None,
-                    help="time only the fp8-decode, block-copy or mixed-round row, for profiling "
-                         "(--num-seqs applies to the fp8 row)")
+    ap.add_argument("--only-row", default=None,
+                    choices=["fp8", "copy", "mixed", "store", "decode_3seq", "decode_64seq",
+                             "decode_longtail"],
+                    help="time only one row (fp8 decode, block copy, mixed round, sustained "
+                         "store, or another decode workload), for profiling (--num-seqs applies "
+                         "to the fp8 row, --store-copies to the store row)")
+    ap.add_argument("--store-copies", type=int, default=16,
+                    help="back-to-back disjoint store launches of the sustained store row")
     return ap.parse_args()
 
 
@@ -70,6 +75,15 @@ def measured_peaks():
             p = json.load(f)
         return float(p["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def measured_bf16_peak():
+    """Dense bf16 GEMM TFLOP/s: the measured burst figure, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
 
 
 # ----------------------------------------------------------------- clocks --
@@ -179,6 +193,19 @@ def decode_bytes(w) -> int:
     ctx = w.context_lens.astype(np.int64)
     return int((ctx * hkv * d * 2 * 2).sum() + w.num_seqs * hq * d * 2 * 2
                + 4 * ((ctx + bs - 1) // bs).sum() + 4 * w.num_seqs)
+
+
+def workload_config(w, world=1) -> dict:
+    """The JSON line's config: the workload and its sizes (both arms print it)."""
+    kv = int((w.context_lens.astype(np.int64) * w.num_kv_heads * w.head_dim * 4).sum())
+    return {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "num_blocks": w.num_blocks,
+            "total_context_tokens": int(w.context_lens.sum()),
+            "kv_bytes_read_per_step": kv,
+            "l2": "inputs larger than L2: every step streams the whole KV context "
+                  f"({kv / 1e9:.2f} GB > 129 MB L2)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def store_bytes(w) -> int:
@@ -359,46 +386,14 @@ def run_pkv(args, rank, world, device):
         raise RuntimeError("device-side range check fired during the timed region")
 
 
-    # end to end through the public API with host buffers: H2D of the step's
-    # inputs from pinned memory, the decode step, D2H of the output. The inputs
-    # travel as one packed buffer (q, new K, new V, block tables, lengths at
-    # 256-byte aligned offsets) so a step makes one copy each way.
-    parts = [("q", t["q"]), ("key", kn), ("value", vn), ("bt", bt), ("cl", cl)]
-    offs, off = {}, 0
-    for k, v in parts:
-        offs[k] = off
-        off += (v.numel() * v.element_size() + 255) // 256 * 256
-    host_pack = torch.empty(off, dtype=torch.uint8).pin_memory()
-    dev_pack = torch.empty(off, dtype=torch.uint8, device=device)
-
-    def view(buf, k, like):
-        n = like.numel() * like.element_size()
-        return buf[offs[k]:offs[k] + n].view(like.dtype).view(like.shape)
-
-    for k, v in parts:
-        view(host_pack, k, v).copy_(v.cpu())
-    dev = {k: view(dev_pack, k, v) for k, v in parts}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for _, v in parts)
-    d2h = host_out.numel() * host_out.element_size()
-
-    def e2e_step():
-        dev_pack.copy_(host_pack, non_blocking=True)
-        pkv.decode_step(dev["q"], dev["key"], dev["value"], t["k_cache"], t["v_cache"],
-                        dev["bt"], dev["cl"], w.scale, out=out, workspace=ws)
-        host_out.copy_(out, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b) / args.steps
+    # end to end through the public API with host buffers: every step copies its
+    # inputs from pinned host memory (q, new K, new V, block tables, lengths as one
+    # packed buffer at 256-byte aligned offsets), runs the decode step, and copies
+    # its output back to pinned host memory. The copies run on two copy streams
+    # with double-buffered device inputs and outputs, ordered by events, so step
+    # k+1's upload and step k-1's download overlap step k's compute; every copy is
+    # inside the timed region.
+    e2e_ms, h2d, d2h = measure_e2e(w, t, kn, vn, bt, cl, ws, out, args.steps, device, barrier)
     e2e_ms = max_over_ranks(e2e_ms, world, device)
 
     peak, peak_kind = measured_peaks()
@@ -409,14 +404,7 @@ def run_pkv(args, rank, world, device):
         "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 values, lognormal context lengths)",
-        "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                   "block_size": w.block_size, "num_blocks": w.num_blocks,
-                   "total_context_tokens": int(w.context_lens.sum()),
-                   "kv_bytes_read_per_step": int((w.context_lens.astype(np.int64) * w.num_kv_heads * w.head_dim * 4).sum()),
-                   "l2": "inputs larger than L2: every step streams the whole KV context "
-                         f"({(w.context_lens.astype(np.int64) * w.num_kv_heads * w.head_dim * 4).sum() / 1e9:.2f} GB > 129 MB L2)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": workload_config(w, world),
         "kv_gbs": achieved,
         "roofline": {"bound": "hbm",
                      "kernel": "pkv_decode_step (plan + new-token store, tcgen05 decode, combine)",
@@ -437,11 +425,217 @@ def run_pkv(args, rank, world, device):
     result["copy_blocks_row"] = measure_copy_blocks(device, steps=max(5, min(args.steps, 20)))
     result["fp8_decode_row"] = measure_fp8_decode(device, steps=max(5, min(args.steps, 20)))
     result["mixed_batch_row"] = measure_mixed(device, steps=max(5, min(args.steps, 20)))
+    result["store_row"] = measure_store_sustained(device)
+    result["decode_config_rows"] = [measure_decode_config(n, device, steps=max(5, min(args.steps, 20)))
+                                    for n in ("decode_3seq", "decode_64seq", "decode_longtail")]
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_oracle_sample(w)
         one = cpu_oracle_sample(w, target_s=5.0, threads=1)   # the same oracle on one core
         result["cpu_baseline"]["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
     return result
+
+
+def measure_e2e(w, t, kn, vn, bt, cl, ws, out, steps, device, barrier=lambda: None):
+    """Mean ms per decode step end to end through the public API with host
+    buffers (see run_pkv), and the bytes copied in and out per step."""
+    import torch
+    import paged_kv_cache_86_gb300 as pkv
+    parts = [("q", t["q"]), ("key", kn), ("value", vn), ("bt", bt), ("cl", cl)]
+    offs, off = {}, 0
+    for k, v in parts:
+        offs[k] = off
+        off += (v.numel() * v.element_size() + 255) // 256 * 256
+    host_pack = torch.empty(off, dtype=torch.uint8).pin_memory()
+
+    def view(buf, k, like):
+        n = like.numel() * like.element_size()
+        return buf[offs[k]:offs[k] + n].view(like.dtype).view(like.shape)
+
+    for k, v in parts:
+        view(host_pack, k, v).copy_(v.cpu())
+    dev_packs = [torch.empty(off, dtype=torch.uint8, device=device) for _ in range(2)]
+    devs = [{k: view(p, k, v) for k, v in parts} for p in dev_packs]
+    outs = [out, torch.empty_like(out)]
+    host_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    h2d = sum(v.numel() * v.element_size() for _, v in parts)
+    d2h = host_outs[0].numel() * host_outs[0].element_size()
+    comp = torch.cuda.current_stream(device)
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+
+    def ev():
+        return torch.cuda.Event()
+
+    def run(n, start=None, end=None):
+        uploaded = [ev(), ev()]     # H2D of step k into pack k % 2 done
+        computed = [ev(), ev()]     # step k (reads pack k % 2, writes outs[k % 2]) done
+        downloaded = [ev(), ev()]   # D2H of outs[k % 2] done
+        fresh = [True, True]
+        if start is not None:
+            start.record(up)
+        with torch.cuda.stream(up):
+            dev_packs[0].copy_(host_pack, non_blocking=True)
+            uploaded[0].record(up)
+        for k in range(n):
+            b = k % 2
+            if k + 1 < n:           # upload step k+1 while step k computes
+                nb = (k + 1) % 2
+                if k >= 1:          # pack nb was read by step k-1
+                    up.wait_event(computed[nb])
+                with torch.cuda.stream(up):
+                    dev_packs[nb].copy_(host_pack, non_blocking=True)
+                    uploaded[nb].record(up)
+            comp.wait_event(uploaded[b])
+            if not fresh[b]:        # outs[b] is still being downloaded (step k-2)
+                comp.wait_event(downloaded[b])
+            d = devs[b]
+            pkv.decode_step(d["q"], d["key"], d["value"], t["k_cache"], t["v_cache"], d["bt"],
+                            d["cl"], w.scale, out=outs[b], workspace=ws)
+            computed[b].record(comp)
+            fresh[b] = False
+            down.wait_event(computed[b])
+            with torch.cuda.stream(down):
+                host_outs[b].copy_(outs[b], non_blocking=True)
+                downloaded[b].record(down)
+        comp.wait_stream(up)
+        comp.wait_stream(down)
+        if end is not None:
+            end.record(comp)
+
+    run(3)
+    torch.cuda.synchronize()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run(steps, a, b)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def decode_kernel_path(w) -> str:
+    """Which attention kernel the library's dispatch picks for this shape (its
+    documented rule: all-heads tcgen05 kernel when Hkv is a power of two >= 4 and
+    128 / Hkv tokens divide the block size; per-head tcgen05 kernel when the block
+    size is a multiple of 8; CUDA-core split kernel otherwise)."""
+    hkv, bs = w.num_kv_heads, w.block_size
+    if hkv >= 4 and hkv & (hkv - 1) == 0 and bs % (128 // hkv) == 0:
+        return "decode_tcg_kernel (tcgen05, all KV heads per stage)"
+    if bs % 8 == 0:
+        return "decode_tc_kernel (tcgen05, one KV head per CTA)"
+    return "decode_split_kernel (CUDA cores)"
+
+
+def measure_decode_config(name, device, steps):
+    """A decode-step row for another decode workload: pkv_decode_step (the new
+    token of every sequence stored, then paged decode) timed with CUDA events.
+    Workloads whose K/V exceed L2 run back to back (every step streams more than
+    L2); smaller ones are timed launch by launch after a clean L2 refill."""
+    import torch
+    import paged_kv_cache_86_gb300 as pkv
+    w = make_workload(name, fill="device")
+    t = {k: v.to(device) for k, v in w.tensors.items()}
+    bt = torch.from_numpy(w.block_tables).to(device)
+    cl = torch.from_numpy(w.context_lens).to(device)
+    assert (w.context_lens > 0).all() and w.num_new_tokens == w.num_seqs
+    out = torch.empty_like(t["q"])
+    ws = torch.empty(pkv.decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        pkv.decode_step(t["q"], t["key"], t["value"], t["k_cache"], t["v_cache"], bt, cl, w.scale,
+                        out=out, workspace=ws)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    nbytes = decode_bytes(w) + store_bytes(w)
+    kv = int((w.context_lens.astype(np.int64) * w.num_kv_heads * w.head_dim * 4).sum())
+    if kv > (256 << 20):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        how = f"back to back, mean of {steps} steps; {kv / 1e9:.2f} GB of K/V per step > L2"
+    else:
+        ms = timed_after_clean_flush(step, steps, device)
+        how = (f"{kv / 1e6:.1f} MB of K/V fits in L2: each step after a clean 256 MiB L2 "
+               f"refill, median of {steps}")
+    if pkv.get_device_errors() != 0:
+        raise RuntimeError(f"device-side range check fired in the {name} measurement")
+    hpeak, kind = measured_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "block_size": w.block_size,
+            "total_context_tokens": int(w.context_lens.sum()),
+            "kernel": decode_kernel_path(w), "ms": ms,
+            "tokens_per_s": w.num_seqs / (ms * 1e-3),
+            "algorithmic_bytes_per_launch": nbytes, "gbs": gbs, "frac_of_hbm": gbs / hpeak,
+            "peak_source": f"{kind} hbm_gbs", "timing": how}
+
+
+def measure_store_sustained(device, copies=16, reps=5):
+    """The store row in the regime where its writes must reach HBM: `copies`
+    disjoint repetitions of the chunked-prefill store (16384 tokens at the
+    workload's slots, each copy in its own region of one large pool, each with
+    its own input rows) launched back to back. Per-launch time is the slope
+    between a run of copies/4 launches and a run of all copies (each run after
+    a clean L2 refill), so the dirty lines a run leaves in L2 at its end event
+    cancel out; the mean over the long run is reported beside it."""
+    import torch
+    import paged_kv_cache_86_gb300 as pkv
+    w = make_workload("prefill_chunks", fill="none")
+    hkv, d, bs = w.num_kv_heads, w.head_dim, w.block_size
+    slots_per_copy = w.num_blocks * bs
+    nb = w.num_blocks * copies
+    kc = torch.empty((nb, bs, hkv, d), dtype=torch.bfloat16, device=device)
+    vc = torch.empty_like(kc)
+    base = torch.from_numpy(w.slot_mapping.astype(np.int64)).to(device)
+    sms = [(base + j * slots_per_copy).to(torch.int32) for j in range(copies)]
+    g = torch.Generator(device=device).manual_seed(86021)
+    keys = torch.empty((copies, w.num_new_tokens, hkv, d), dtype=torch.bfloat16,
+                       device=device).normal_(generator=g)
+    vals = torch.empty_like(keys).normal_(generator=g)
+    stream = torch.cuda.current_stream(device)
+
+    def run(n):
+        for j in range(n):
+            pkv.store_kvcache(keys[j], vals[j], kc, vc, sms[j])
+
+    run(copies)
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush_rd = torch.ones(64 << 20, dtype=torch.float32, device=device)
+    short = max(1, copies // 4)
+    times = {short: [], copies: []}
+    for _ in range(reps):
+        for n in (short, copies):
+            flush.zero_()
+            flush_rd.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run(n)
+            b.record(stream)
+            torch.cuda.synchronize()
+            times[n].append(a.elapsed_time(b))
+    if pkv.get_device_errors() != 0:
+        raise RuntimeError("device-side range check fired in the store measurement")
+    t_short, t_long = statistics.median(times[short]), statistics.median(times[copies])
+    slope = (t_long - t_short) / (copies - short)
+    sb = store_bytes(w)
+    hpeak, kind = measured_peaks()
+    return {"workload": f"{copies} x store of {w.num_new_tokens} chunk tokens "
+                        f"({w.name} slots) into disjoint pool regions",
+            "algorithmic_bytes_per_launch": sb,
+            "ms_per_launch": slope, "gbs": sb / (slope * 1e-3) / 1e9,
+            "frac_of_hbm": sb / (slope * 1e-3) / 1e9 / hpeak,
+            "ms_per_launch_mean_of_long_run": t_long / copies,
+            "frac_of_hbm_mean_of_long_run": sb / (t_long / copies * 1e-3) / 1e9 / hpeak,
+            "peak_source": f"{kind} hbm_gbs",
+            "timing": f"slope between {short} and {copies} back-to-back launches, medians of "
+                      f"{reps} runs, each run after a clean 256 MiB L2 refill; "
+                      f"{copies * sb / 2e9:.2f} GB written per long run (> L2)"}
 
 
 def fp8_decode_bytes(w) -> int:
@@ -573,40 +767,89 @@ def measure_mixed(device, steps):
     if pkv.get_device_errors() != 0:
         raise RuntimeError("device-side range check fired in the mixed-batch measurement")
     tokens = int(w.num_q_rows)
-    return {"workload": w.name, "scheduled_tokens": tokens, "ms": res["mixed_step"],
-            "tokens_per_s": tokens / (res["mixed_step"] * 1e-3),
+    # the round's floors: decode rows are HBM-bound (K/V once per KV head, q,
+    # out, tables), chunk rows tensor-bound (causal-region FLOPs), and every new
+    # token is stored (its K/V rows read and written)
+    hkv, hq, dd, bs = w.num_kv_heads, w.num_q_heads, w.head_dim, w.block_size
+    ctx = w.context_lens[:d].astype(np.int64)
+    dec_bytes = int((ctx * hkv * dd * 4).sum() + d * hq * dd * 4
+                    + (4 * ((ctx + bs - 1) // bs)).sum() + 4 * d)
+    q_lens, k_lens = w.q_lens[d:].astype(np.int64), w.context_lens[d:].astype(np.int64)
+    chunk_flops = sum(4 * dd * hq * int(((k - q) + np.arange(1, q + 1)).sum())
+                      for q, k in zip(q_lens, k_lens))
+    chunk_bytes = int((k_lens * hkv * dd * 4).sum() + q_lens.sum() * hq * dd * 4)
+    st_bytes = store_bytes(w)
+    hpeak, _ = measured_peaks()
+    tpeak = measured_bf16_peak()
+    hbm_ms = (dec_bytes + st_bytes) / (hpeak * 1e9) * 1e3
+    tensor_ms = chunk_flops / (tpeak * 1e12) * 1e3
+    floor_serial = hbm_ms + tensor_ms
+    floor_overlap = max((dec_bytes + st_bytes + chunk_bytes) / (hpeak * 1e9) * 1e3, tensor_ms)
+    ms = res["mixed_step"]
+    return {"workload": w.name, "scheduled_tokens": tokens, "ms": ms,
+            "tokens_per_s": tokens / (ms * 1e-3),
             "ms_all_through_prefill_kernel": res["store_plus_prefill_kernel_for_all"],
+            "roofline": {"decode_bytes": dec_bytes, "store_bytes": st_bytes,
+                         "chunk_flops": chunk_flops, "chunk_kv_q_out_bytes": chunk_bytes,
+                         "floor_ms_serial": floor_serial, "frac_serial": floor_serial / ms,
+                         "floor_ms_overlapped": floor_overlap,
+                         "frac_overlapped": floor_overlap / ms,
+                         "how": "serial floor: decode rows' and stores' bytes at the measured HBM "
+                                "peak, then the chunks' causal FLOPs at the measured bf16 burst "
+                                "peak; overlapped floor: the larger of all bytes at the HBM peak "
+                                "and the FLOPs at the bf16 peak"},
             "l2": "K/V of the round larger than L2 (~1 GB); each launch after a clean 256 MiB "
                   "L2 refill; median of launches"}
 
 
-def measure_copy_blocks(device, steps):
+def measure_copy_blocks(device, steps, launches=8):
     """The copy-on-write row: 4096 whole-block copies (random distinct source and
     destination blocks of a 16-token, 8-KV-head pool), K and V: 512 MiB moved per
-    launch, more than L2, timed with CUDA events."""
+    launch. Timed two ways: one launch after a clean L2 refill (median of
+    `steps`), and per launch as the slope between 2 and `launches` back-to-back
+    launches over disjoint block pairs, where every launch's writes must reach
+    HBM (the dirty lines left in L2 at a run's end event cancel out)."""
     import torch
     import paged_kv_cache_86_gb300 as pkv
-    nb, bs, hkv, d, pairs = 16384, 16, 8, 128, 4096
+    bs, hkv, d, pairs = 16, 8, 128, 4096
+    nb = 2 * pairs * launches
     g = torch.Generator(device=device).manual_seed(86009)
     kc = torch.empty((nb, bs, hkv, d), dtype=torch.bfloat16, device=device).normal_(generator=g)
     vc = torch.empty_like(kc).normal_(generator=g)
-    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(86010))
-    src = perm[:pairs].to(torch.int32).to(device)
-    dst = perm[pairs:2 * pairs].to(torch.int32).to(device)
-    for _ in range(3):
-        pkv.copy_blocks(kc, vc, src, dst)
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(86010)).to(torch.int32)
+    srcs = [perm[2 * j * pairs:(2 * j + 1) * pairs].to(device) for j in range(launches)]
+    dsts = [perm[(2 * j + 1) * pairs:(2 * j + 2) * pairs].to(device) for j in range(launches)]
+    for j in range(launches):
+        pkv.copy_blocks(kc, vc, srcs[j], dsts[j])
     torch.cuda.synchronize()
-    ms = timed_after_clean_flush(lambda: pkv.copy_blocks(kc, vc, src, dst), steps, device)
+    ms = timed_after_clean_flush(lambda: pkv.copy_blocks(kc, vc, srcs[0], dsts[0]), steps, device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush_rd = torch.ones(64 << 20, dtype=torch.float32, device=device)
+    runs = {2: [], launches: []}
+    for _ in range(5):
+        for n in runs:
+            flush.zero_()
+            flush_rd.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for j in range(n):
+                pkv.copy_blocks(kc, vc, srcs[j], dsts[j])
+            b.record(stream)
+            torch.cuda.synchronize()
+            runs[n].append(a.elapsed_time(b))
     if pkv.get_device_errors() != 0:
         raise RuntimeError("device-side range check fired in the block-copy measurement")
+    slope = (statistics.median(runs[launches]) - statistics.median(runs[2])) / (launches - 2)
     nbytes = pairs * 2 * 2 * bs * hkv * d * 2      # K and V, read and write
     hpeak, _ = measured_peaks()
     return {"workload": f"copy_{pairs}_blocks_bs{bs}_hkv{hkv}", "bytes_per_launch": nbytes,
-            "ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
-            "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hpeak,
-            "l2": "512 MiB per launch, larger than L2; each launch after a clean 256 MiB L2 refill; "
-                  "median of launches; up to one L2 of the copy's writes (ncu: ~50 MB) is still "
-                  "being written back when the end event fires"}
+            "ms_per_launch": slope, "gbs": nbytes / (slope * 1e-3) / 1e9,
+            "frac_of_hbm": nbytes / (slope * 1e-3) / 1e9 / hpeak,
+            "timing": f"slope between 2 and {launches} back-to-back launches over disjoint block "
+                      "pairs, medians of 5 runs, each run after a clean 256 MiB L2 refill",
+            "ms_single_launch_after_clean_l2": ms,
+            "frac_of_hbm_single_launch": nbytes / (ms * 1e-3) / 1e9 / hpeak}
 
 
 def prefill_flops(w) -> int:
@@ -697,8 +940,11 @@ def measure_prefill(args, device, steps):
     sb = store_bytes(w)
     return {"workload": w.name,
             "l2": "256 MiB written then 256 MiB read before each launch (clean L2); median of launches",
-            "store_ms": res["store"], "store_gbs": sb / (res["store"] * 1e-3) / 1e9,
-            "store_frac_of_hbm": sb / (res["store"] * 1e-3) / 1e9 / hpeak,
+            "store_note": "one 16384-token store launch: its 67 MB of writes fit in L2, so a "
+                          "clean-L2 launch can end before they reach HBM; store_row gives the "
+                          "sustained figure",
+            "store_ms_single_launch_clean_l2": res["store"],
+            "store_frac_of_hbm_single_launch_clean_l2": sb / (res["store"] * 1e-3) / 1e9 / hpeak,
             "store_ms_after_write_only_flush": res["store_dirty_l2"],
             "store_frac_of_hbm_after_write_only_flush": sb / (res["store_dirty_l2"] * 1e-3) / 1e9 / hpeak,
             "prefill_ms": res["prefill"], "prefill_tflops": fl / (res["prefill"] * 1e-3) / 1e12,
@@ -717,7 +963,7 @@ def run_reference(args, rank):
         cpu_oracle_sample(w, target_s=0.5, max_seqs=8)
     samples = []
     for _ in range(args.steps):
-        r = cpu_oracle_sample(w, target_s=max(1.0, 120.0 / max(args.steps, 1)), max_seqs=None)
+        r = cpu_oracle_sample(w, target_s=max(1.0, 60.0 / max(args.steps, 1)), max_seqs=None)
         samples.append(r)
         per_step.append(r["value"])
     value = statistics.mean(per_step)
@@ -727,7 +973,8 @@ def run_reference(args, rank):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.num_seqs / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded N(0,1) bf16)", "config": {"workload": w.name},
+            "data": "synthetic (seeded N(0,1) bf16 values, lognormal context lengths)",
+            "config": workload_config(w),
             "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -763,6 +1010,10 @@ def main():
             res = {"fp8_decode_row": measure_fp8_decode(device, steps, num_seqs=args.num_seqs)}
         elif args.only_row == "copy":
             res = {"copy_blocks_row": measure_copy_blocks(device, steps)}
+        elif args.only_row == "store":
+            res = {"store_row": measure_store_sustained(device, copies=args.store_copies)}
+        elif args.only_row.startswith("decode_"):
+            res = {"decode_config_row": measure_decode_config(args.only_row, device, steps)}
         else:
             res = {"mixed_batch_row": measure_mixed(device, steps)}
     else:

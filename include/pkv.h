@@ -48,6 +48,14 @@
  * that is out of range is skipped (never dereferenced), its output is
  * unspecified, and a bit is set in a per-device error word that
  * pkv_get_device_errors() returns and clears.
+ *
+ * Device state. The library keeps two pieces of state per device: the error
+ * word and, for pkv_paged_decode_static_ws, the address of its scratch array.
+ * Both are `__device__` variables of the library's module; their addresses are
+ * looked up once per device (first use, with that device current) and kept.
+ * Destroying the device's primary context while the library is loaded
+ * (cudaDeviceReset, or the driver API's primary-context reset) invalidates
+ * them: do not reset a device between calls into this library.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -326,7 +334,8 @@ pkv_status pkv_decode_step(void *out, const void *q,
  *   PKV_ERR_WORKSPACE before anything is launched.
  *   Set-up: the first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current and caches it; make that
- *   first call before any stream capture.
+ *   first call before any stream capture, and do not reset the device while
+ *   the library is loaded (the cached address would be stale).
  *   Sharing: all calls share the one array and it keeps the last call's
  *   contents (nothing in it needs to start at zero). Calls whose kernels may
  *   overlap on the GPU (different streams without ordering) race on it; order

@@ -102,13 +102,27 @@ def _stream(t: torch.Tensor, stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _need(t: torch.Tensor, name: str, dtype, ndim=None):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor")
+def _need(t: torch.Tensor, name: str, dtype, ndim=None, contiguous=False, on_gpu=True):
+    """dtype, rank and (optionally) dense row-major layout, then the device (unless
+    on_gpu is False: the caller checks every tensor's device after every layout).
+    The kernels take a raw pointer and assume the layout, so a strided view would
+    be misread."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dimensions, got {t.dim()}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if on_gpu:
+        _need_gpu((t, name))
+
+
+def _need_gpu(*named):
+    for t, name in named:
+        if not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
 
 
 def _out_like(out, q: torch.Tensor) -> torch.Tensor:
@@ -276,18 +290,21 @@ def mixed_step(q, key, value, slot_mapping, k_cache, v_cache, cu_seqlens_q, cu_s
     query row each (rows 0..D-1), the rest prefill chunks; every query row's K/V
     (key / value [total_q, Hkv, D]) is stored at slot_mapping first. Returns out
     [total_q, Hq, D] bf16."""
-    lib = load()
-    _need(q, "q", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3, contiguous=True, on_gpu=False)
     for t, n in ((key, "key"), (value, "value")):
-        _need(t, n, torch.bfloat16, 3)
+        _need(t, n, torch.bfloat16, 3, on_gpu=False)
         if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
             raise ValueError(f"{n} rows must be contiguous [Hkv, D] blocks")
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t, n, torch.bfloat16, 4)
+        _need(t, n, torch.bfloat16, 4, contiguous=True, on_gpu=False)
     for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k"),
                  (slot_mapping, "slot_mapping")):
-        _need(t, n, torch.int32, 1)
-    _need(block_tables, "block_tables", torch.int32, 2)
+        _need(t, n, torch.int32, 1, contiguous=True, on_gpu=False)
+    _need(block_tables, "block_tables", torch.int32, 2, contiguous=True, on_gpu=False)
+    _need_gpu((q, "q"), (key, "key"), (value, "value"), (k_cache, "k_cache"),
+              (v_cache, "v_cache"), (cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k"),
+              (slot_mapping, "slot_mapping"), (block_tables, "block_tables"))
+    lib = load()
     total_q, hq, d = q.shape
     nb, bs, hkv, _ = k_cache.shape
     s = cu_seqlens_q.shape[0] - 1
@@ -433,13 +450,16 @@ def paged_prefill(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables,
                   max_seqlen_q: int, max_seqlen_k: int, causal: bool = True, out=None,
                   workspace=None, stream=None) -> torch.Tensor:
     """Varlen chunked-prefill attention; returns out [total_q, Hq, D] bf16."""
-    lib = load()
-    _need(q, "q", torch.bfloat16, 3)
+    named = ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (cu_seqlens_q, "cu_seqlens_q"),
+             (cu_seqlens_k, "cu_seqlens_k"), (block_tables, "block_tables"))
+    _need(q, "q", torch.bfloat16, 3, contiguous=True, on_gpu=False)
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t, n, torch.bfloat16, 4)
+        _need(t, n, torch.bfloat16, 4, contiguous=True, on_gpu=False)
     for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
-        _need(t, n, torch.int32, 1)
-    _need(block_tables, "block_tables", torch.int32, 2)
+        _need(t, n, torch.int32, 1, contiguous=True, on_gpu=False)
+    _need(block_tables, "block_tables", torch.int32, 2, contiguous=True, on_gpu=False)
+    _need_gpu(*named)
+    lib = load()
     total_q, hq, d = q.shape
     nb, bs, hkv, _ = k_cache.shape
     s = cu_seqlens_q.shape[0] - 1

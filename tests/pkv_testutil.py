@@ -11,6 +11,12 @@ from paged_kv_cache_86_gb300.workloads import Workload, bf16_to_u16
 
 RTOL = 1e-2  # |gpu - oracle| <= RTOL * max(1, |oracle|), elementwise
 
+# Every comparison's worst |err| / bound, with the test that made it; the
+# conftest prints them at the end of the session so the margin to the
+# tolerance can be read from the log.
+MARGINS: list = []
+CURRENT_TEST = {"id": ""}
+
 
 def device_meta(w: Workload, device="cuda") -> dict:
     d = {
@@ -94,11 +100,15 @@ def assert_close(gpu: torch.Tensor, ref: np.ndarray, what: str = ""):
     assert np.isfinite(g).all(), f"{what}: non-finite GPU output"
     err = np.abs(g - ref)
     bound = RTOL * np.maximum(1.0, np.abs(ref))
+    ratio = float((err / bound).max()) if err.size else 0.0
+    MARGINS.append({"test": CURRENT_TEST["id"], "what": what, "elements": int(err.size),
+                    "max_err": float(err.max()) if err.size else 0.0, "ratio": ratio})
     bad = err > bound
     if bad.any():
         idx = np.argwhere(bad)[:5]
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements beyond tolerance; "
-                             f"max err {err.max():.3e}; first at {idx.tolist()}")
+                             f"max err {err.max():.3e}; worst |err|/bound {ratio:.3f}; "
+                             f"first at {idx.tolist()}")
     return float(err.max())
 
 

@@ -68,14 +68,23 @@ def test_mixed_step_flags_a_decode_sequence_with_two_rows():
     assert pkv.get_device_errors() & pkv._lib.DEVERR_LENGTH
 
 
-def test_mixed_step_full_size_sampled():
+def test_mixed_step_full_size_decode_rows_and_chunk_tiles():
+    """A full-size round: every decode row, every row of two of the chunks, and
+    the first and last row of every 128-row tile of the others."""
     rng = np.random.default_rng(13)
     dec = np.clip(np.rint(np.exp(np.log(800) + rng.standard_normal(256))), 16, 4096).astype(int)
     w, d = mixed_workload("mixed_256d_8x512", dec.tolist(), [512] * 8,
                           rng.integers(0, 3585, 8).tolist(), 32, 8, 16, seed=14)
     t = {k: v.cuda() for k, v in w.tensors.items()}
     mask = np.zeros(w.num_q_rows, np.uint8)
-    rows = np.concatenate([rng.choice(d, 12, replace=False), d + rng.choice(w.num_q_rows - d, 40, replace=False)])
+    cu = w.cu_seqlens_q
+    rows = set(range(d))
+    for i in range(d, w.num_seqs):
+        if i < d + 2:
+            rows |= set(range(int(cu[i]), int(cu[i + 1])))
+        for r0 in range(int(cu[i]), int(cu[i + 1]), 128):
+            rows |= {r0, min(r0 + 127, int(cu[i + 1]) - 1)}
+    rows = np.array(sorted(rows))
     mask[rows] = 1
     ref = prefill_step_reference(w, t["k_cache"], t["v_cache"], t["q"], t["key"], t["value"], row_mask=mask)
     out, _ = run_mixed(w, d, t)

@@ -96,10 +96,19 @@ def test_prefill_last_row_matches_decode():
     assert diff.max().item() <= 2e-2 * max(1.0, dec.float().abs().max().item())
 
 
-def test_prefill_full_size_sampled_rows():
+def test_prefill_full_size_whole_chunks_and_every_tile_boundary():
+    """The 32 x 512 chunked workload at full size: every row of 8 of its chunks
+    (the 4 longest and 4 shortest prefixes), and in all 32 chunks the first and
+    last row of every 128-row query tile."""
     w = W.prefill_chunks()
     assert w.num_q_rows == 16384
-    rng = np.random.default_rng(5)
-    rows = set(rng.choice(w.num_q_rows, size=96, replace=False).tolist())
-    rows |= set(w.cu_seqlens_q[:-1].tolist()) | set((w.cu_seqlens_q[1:] - 1).tolist())
+    cu = w.cu_seqlens_q
+    order = np.argsort(w.context_lens)
+    whole = list(order[:4]) + list(order[-4:])
+    rows = set()
+    for i in whole:
+        rows |= set(range(int(cu[i]), int(cu[i + 1])))
+    for i in range(w.num_seqs):
+        for r0 in range(int(cu[i]), int(cu[i + 1]), 128):
+            rows |= {r0, min(r0 + 127, int(cu[i + 1]) - 1)}
     check(w, rows=sorted(rows))
