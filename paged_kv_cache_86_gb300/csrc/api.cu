@@ -167,7 +167,11 @@ pkv_status decode_call(void *out, const void *q, const void *key_new, const void
     return PKV_ERR_ARG;
   if (head_dim != 128) return PKV_ERR_SHAPE;
   if (int64_t(max_context_len) > int64_t(max_blocks_per_seq) * block_size) return PKV_ERR_ARG;
-  if (int64_t(num_seqs) * max_context_len * num_kv_heads >= (int64_t(1) << 31)) return PKV_ERR_ARG;
+  // the flat space the CTA ranges cut (int32 on the device): every token, once
+  // per KV head on the per-head kernel, plus the per-segment units of the plan
+  if (int64_t(num_seqs) * (int64_t(max_context_len) + pkv::kDecodeSegmentCost) * num_kv_heads >=
+      (int64_t(1) << 31))
+    return PKV_ERR_ARG;
   if (num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !context_lens ||
       (!block_tables && max_blocks_per_seq > 0))

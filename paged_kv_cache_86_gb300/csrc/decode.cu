@@ -123,8 +123,8 @@ struct NewTokens {
 
 __global__ void __launch_bounds__(1024)
 decode_plan_kernel(const int32_t *__restrict__ context_lens, int num_seqs, int max_context_len,
-                   int grid, int units_per_token, int min_range, uint8_t *ws, uint32_t *err,
-                   NewTokens nt) {
+                   int grid, int units_per_token, int min_range, int seg_cost, uint8_t *ws,
+                   uint32_t *err, NewTokens nt) {
   __shared__ int warp_sums[32];
   __shared__ int base;
   int *cu = reinterpret_cast<int *>(ws + 256);
@@ -188,7 +188,9 @@ decode_plan_kernel(const int32_t *__restrict__ context_lens, int num_seqs, int m
         x = x < 0 ? 0 : max_context_len;
       }
     }
-    int v = x;
+    // a non-empty sequence takes seg_cost units of the flat space in front of
+    // its tokens (the fixed cost of a segment, so ranges balance time)
+    int v = x > 0 ? x + seg_cost : 0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int y = __shfl_up_sync(kFull, v, off);
@@ -591,6 +593,7 @@ struct CombineParams {
   int grid;
   int tc;      // records of the tcgen05 kernel: one row per (slot, query head of the group)
   int group;
+  int seg_cost;  // units in front of each non-empty sequence in the flat space (see the plan)
 };
 
 // One warp per (sequence, query head); lane l owns dims 4l .. 4l+3. The
@@ -628,12 +631,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   const int qh = gw - i * p.num_q_heads;
   const Header hdr = *reinterpret_cast<const Header *>(p.ws);
   const int *cu = reinterpret_cast<const int *>(p.ws + 256);
-  const int c0 = cu[i], c1 = cu[i + 1];
+  const int v0 = cu[i], c1 = cu[i + 1];
   uint2 *orow = reinterpret_cast<uint2 *>(p.out + (static_cast<size_t>(i) * p.num_q_heads + qh) * kHeadDim);
-  if (c1 == c0) {  // empty context: zero row
+  if (c1 == v0) {  // empty context: zero row
     orow[lane] = make_uint2(0u, 0u);
     return;
   }
+  const int c0 = v0 + p.seg_cost;  // first token of the sequence in the flat space
   // position of this (head, sequence) in the flat space the CTA ranges cut
   const long long start = p.tc ? static_cast<long long>(qh / p.group) * hdr.total + c0 : c0;
   const long long b_first = start / hdr.range;
@@ -663,13 +667,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
         wk = ml.y * fast_exp2(ml.x - m_max);
       }
       const int cnt = min(32, n - base);
-#pragma unroll 4
-      for (int k = 0; k < cnt; ++k) {
-        const float wgt = __shfl_sync(kFull, wk, k);
-        const long long row = __shfl_sync(kFull, row_k, k);
-        const float4 v = reinterpret_cast<const float4 *>(p.po + row * kHeadDim)[lane];
-        o.x += wgt * v.x; o.y += wgt * v.y; o.z += wgt * v.z; o.w += wgt * v.w;
-        l_tot += wgt;
+      // eight records per pass, all eight loads issued before the sums (the
+      // partials sit in L2; the latency of one load per record would add up)
+      for (int k0 = 0; k0 < cnt; k0 += 8) {
+        float4 v[8];
+        float wgt[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int k = min(k0 + u, cnt - 1);  // past the end: a valid row, weight 0
+          wgt[u] = __shfl_sync(kFull, wk, k);
+          const long long row = __shfl_sync(kFull, row_k, k);
+          v[u] = reinterpret_cast<const float4 *>(p.po + row * kHeadDim)[lane];
+          if (k0 + u >= cnt) wgt[u] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          o.x += wgt[u] * v[u].x; o.y += wgt[u] * v[u].y;
+          o.z += wgt[u] * v[u].z; o.w += wgt[u] * v[u].w;
+          l_tot += wgt[u];
+        }
       }
     }
   }
@@ -745,7 +761,7 @@ cudaError_t launch_mixed_decode_lens(const int32_t *cu_q, const int32_t *cu_k, i
 // The plan launch: CTA 0 plans the ranges; with new tokens (decode step), CTAs
 // 1.. write them, 32 sequences per CTA.
 cudaError_t launch_plan(const DecodeArgs &a, int grid, int units_per_token, int min_range,
-                        uint8_t *ws, cudaStream_t stream) {
+                        int seg_cost, uint8_t *ws, cudaStream_t stream) {
   NewTokens nt{};
   unsigned ctas = 1;
   if (a.key_new != nullptr) {
@@ -767,7 +783,8 @@ cudaError_t launch_plan(const DecodeArgs &a, int grid, int units_per_token, int 
     ctas += static_cast<unsigned>((a.num_seqs + kStoreSeqsPerCta - 1) / kStoreSeqsPerCta);
   }
   decode_plan_kernel<<<ctas, 1024, 0, stream>>>(a.context_lens, a.num_seqs, a.max_context_len,
-                                                grid, units_per_token, min_range, ws, a.err, nt);
+                                                grid, units_per_token, min_range, seg_cost, ws,
+                                                a.err, nt);
   return cudaGetLastError();
 }
 
@@ -850,15 +867,18 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
   cp.grid = grid;
   cp.group = group;
   cp.tc = plan.tc ? 1 : 0;
+  cp.seg_cost = 0;
 
   if (plan.kind == 3) {
     const WsLayout lay = ws_layout(a.num_seqs, a.num_q_heads, 1, grid);
-    if ((e = launch_plan(a, grid, 1, 128, ws, stream)) != cudaSuccess) return e;
+    if ((e = launch_plan(a, grid, 1, 128, kDecodeSegmentCost, ws, stream)) != cudaSuccess) return e;
     cp.wph = 1;
+    cp.seg_cost = kDecodeSegmentCost;
     cp.ml = reinterpret_cast<float2 *>(ws + lay.ml);
     cp.po = reinterpret_cast<float *>(ws + lay.o);
     if ((e = launch_decode_tcg(a, grid, reinterpret_cast<float2 *>(ws + lay.ml),
-                               reinterpret_cast<float *>(ws + lay.o), stream)) != cudaSuccess)
+                               reinterpret_cast<float *>(ws + lay.o), kDecodeSegmentCost, stream)) !=
+        cudaSuccess)
       return e;
     // mixed batch: the prefill runs on the SMs the attention kernel leaves as
     // its CTAs finish; the combine below waits for the prefill, which waits
@@ -866,7 +886,7 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
     if (a.interleave != nullptr && (e = launch_paged_prefill(*a.interleave, stream)) != cudaSuccess)
       return e;
   } else if (plan.kind == 2) {
-    if ((e = launch_plan(a, grid, a.num_kv_heads, 128, ws, stream)) != cudaSuccess) return e;
+    if ((e = launch_plan(a, grid, a.num_kv_heads, 128, 0, ws, stream)) != cudaSuccess) return e;
     const size_t ml = align256(256 + sizeof(int) * (size_t(a.num_seqs) + 1));
     const size_t o = align256(ml + sizeof(float2) * size_t(2) * grid * group);
     cp.ml = reinterpret_cast<float2 *>(ws + ml);
@@ -876,7 +896,7 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
       return e;
   } else {
     const WsLayout lay = ws_layout(a.num_seqs, a.num_q_heads, wph, grid);
-    if ((e = launch_plan(a, grid, 1, kMinRange, ws, stream)) != cudaSuccess) return e;
+    if ((e = launch_plan(a, grid, 1, kMinRange, 0, ws, stream)) != cudaSuccess) return e;
     SplitParams sp;
     sp.out = static_cast<__nv_bfloat16 *>(a.out);
     sp.q = static_cast<const __nv_bfloat16 *>(a.q);

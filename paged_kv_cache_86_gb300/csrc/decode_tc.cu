@@ -452,11 +452,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
       for (int g = 0; g < kN; ++g) {
         if (g < G) {
-          const float pv = valid ? ex2(sc[g] - m_run[g]) : 0.f;
+          // the weight is rounded to bf16 before it enters the row sum, so the
+          // sum matches the weights the PV MMA multiplies
+          const __nv_bfloat16 hb = __float2bfloat16_rn(valid ? ex2(sc[g] - m_run[g]) : 0.f);
+          const float pv = __bfloat162float(hb);
           l_part[g] = (first ? 0.f : l_part[g] * alpha[g]) + pv;
           const uint32_t addr = prow_base + (g >> 3) * 1024 + (g & 7) * 128 +
                                 ((((tc >> 3) ^ (g & 7)) << 4) | ((tc & 7) << 1));
-          const __nv_bfloat16 hb = __float2bfloat16_rn(pv);
           asm volatile("st.shared.b16 [%0], %1;" :: "r"(addr),
                        "h"(*reinterpret_cast<const unsigned short *>(&hb)) : "memory");
         }

@@ -107,6 +107,7 @@ struct GParams {
   uint32_t *err;
   const float *k_scales;  // fp8 caches: [NB * bs, Hkv] row scales
   const float *v_scales;
+  int seg_cost;           // units in front of each non-empty sequence in the flat space
 };
 
 // shared-memory map, all offsets from a 1024-aligned base
@@ -544,9 +545,12 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (cu[m + 1] > lo) b = m; else a = m + 1;
       }
       for (int i = a; ok && i < p.num_seqs; ++i) {
-        const int c0 = cu[i], c1 = cu[i + 1];
+        // the sequence occupies [cu[i], cu[i+1]) of the flat space: seg_cost
+        // units that stand for the fixed cost of a segment, then its tokens
+        // [c0, c1); a range that ends before c0 has none of its tokens
+        if (cu[i + 1] == cu[i]) continue;
+        const int c0 = cu[i] + p.seg_cost, c1 = cu[i + 1];
         if (c0 >= hi) break;
-        if (c1 == c0) continue;
         GDesc d;
         d.seq = i;
         d.p0 = max(lo, c0) - c0;
@@ -1005,11 +1009,15 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (end) break;
       if (!ok) continue;  // the next stage's barrier takes every warp out
 
-      // P^T values and running row sums
+      // P^T values and running row sums. bf16: each weight is rounded to bf16
+      // before it is summed, so the row sum is the sum of exactly the weights
+      // the PV MMA multiplies (the normalised output is then a convex
+      // combination of the V rows whatever the rounding)
       float pr[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         pr[g] = valid ? ex2(sc[g] - m_used[g]) : 0.f;
+        if (!F8) pr[g] = __bfloat162float(__float2bfloat16_rn(pr[g]));
         l_part[g] = first ? pr[g] : l_part[g] + pr[g];
       }
       const uint32_t p_region = sP + buf * 2 * small + p_half;
@@ -1167,7 +1175,7 @@ bool decode_tcg_supported(int num_q_heads, int num_kv_heads, int block_size, boo
   return block_size % T == 0 && pick_stages(n_cols, fp8) > 0;
 }
 
-cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *po,
+cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *po, int seg_cost,
                               cudaStream_t stream) {
   const int n_cols = (a.num_q_heads + 15) / 16 * 16;
   const bool f8 = a.fp8;
@@ -1218,6 +1226,7 @@ cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *
   p.err = a.err;
   p.k_scales = a.k_scales;
   p.v_scales = a.v_scales;
+  p.seg_cost = seg_cost;
   auto kern = tcg_kernel_for(T, p.group, f8);
   if (kern == nullptr) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -97,7 +97,19 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
 
 // tcgen05 decode kernel, all KV heads of a block per stage (decode_tcg.cu)
 bool decode_tcg_supported(int num_q_heads, int num_kv_heads, int block_size, bool fp8 = false);
-cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *po,
+// The all-heads tcgen05 decode kernel splits the concatenated contexts into
+// equal CTA ranges; every sequence segment a CTA handles also costs a fixed
+// amount of time (its first stage's Q load and reference maximum, its last
+// stage's row sums, output rows and partly filled stage). The plan counts that
+// cost as this many extra tokens in front of each non-empty sequence, so that
+// a CTA given many short sequences gets fewer tokens. Measured on GB300 over
+// 0, 16, 32, 64 and 128: 64 was best for the 512-sequence lognormal batch
+// (386 -> 378 us) and near best for 8 x 32768 + 248 x 200 (230 -> 206 us).
+constexpr int kDecodeSegmentCost = 64;
+
+// seg_cost: extra units the plan put in front of each non-empty sequence's
+// tokens in the flat space the CTA ranges cut (decode.cu, launch_paged_decode)
+cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *po, int seg_cost,
                               cudaStream_t stream);
 
 // tcgen05 decode kernel, one KV head per CTA range (decode_tc.cu)
