@@ -3,9 +3,9 @@
 
 A step is the whole hot path for one batch: store each sequence's new K/V token
 into the cache, then paged decode attention over every sequence's cached
-context, both through one pkv_decode_step call (a plan launch that also writes
-the new tokens, the attention kernel, the combine). The two-call path (pkv_store_kvcache + pkv_paged_decode) is
-timed beside it for the breakdown.
+context, both through one pkv_decode_step call (the attention kernel, which
+plans the call and writes the new tokens, then the combine). The two-call path
+(pkv_store_kvcache + pkv_paged_decode) is timed beside it for the breakdown.
 
 Default workload: 512 sequences, context lengths clip(rint(exp(ln 800 +
 N(0,1))), 16, 4096), 32 query / 8 KV heads, head_dim 128, block size 16, a
@@ -165,9 +165,10 @@ def make_workload(name, seed_offset=0, fill="device", num_seqs=None):
 
 
 def decode_step_launches(w) -> int:
-    """Kernels one pkv_decode_step launches: plan (which also writes the new
-    tokens), attention, combine."""
-    return 3
+    """Kernels one pkv_decode_step launches on the all-heads tcgen05 path: the
+    attention kernel (which plans the call and writes the new tokens) and the
+    combine."""
+    return 2
 
 
 def max_over_ranks(x, world, device):

@@ -298,9 +298,10 @@ pkv_status pkv_paged_decode(void *out, const void *q,
  * Sequence: last_block_num_tokens; §3.2.4 may_append: the last block is the
  * one being written), and then attended to. Sequences with n_i == 0 store
  * nothing and get a zero row. The result equals pkv_store_kvcache with those
- * slots followed by pkv_paged_decode, in the same three launches as
- * pkv_paged_decode alone: the rows are written by the decode's planning
- * launch, beside the range planning.
+ * slots followed by pkv_paged_decode, in the launches of pkv_paged_decode
+ * alone: with bf16 caches on the all-heads tcgen05 kernel the attention kernel
+ * writes each row just before it loads the stage that holds it; otherwise
+ * the decode's planning launch writes the rows beside the range planning.
  * A block id outside [0, num_blocks) skips the write and sets
  * PKV_DEVERR_BLOCK_ID.
  * Graphs: the launches depend only on the host arguments, so a call can be

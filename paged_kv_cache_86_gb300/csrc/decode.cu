@@ -8,7 +8,8 @@
 // byte exactly once at full HBM bandwidth with all SMs busy whatever the
 // length mix.
 //
-// Three launches on the caller's stream:
+// Three launches on the caller's stream (the all-heads tcgen05 kernel of
+// decode_tcg.cu with bf16 caches plans the call itself: two launches):
 //   1. plan     one CTA: prefix sums cu[i] of the (range-checked) context
 //               lengths and the token-range size W = ceil(total / grid)
 //               (rounded up to 16, at least 64).
@@ -831,6 +832,9 @@ bool choose_decode_plan(int num_q_heads, int num_kv_heads, int block_size, Decod
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                               const DecodePlan &plan) {
   if (plan.kind == 2) return tc_workspace(num_seqs, num_q_heads / num_kv_heads, plan.grid);
+  if (plan.kind == 3)  // + the prefix sums of CTAs 1.. (each CTA plans the call itself)
+    return ws_layout(num_seqs, num_q_heads, 1, plan.grid).total +
+           align256(sizeof(int) * size_t(plan.grid - 1) * tcg_cu_stride(num_seqs));
   const int wph = plan.kind == 1 ? kConsumerWarps / num_kv_heads : 1;
   return ws_layout(num_seqs, num_q_heads, wph, plan.grid).total;
 }
@@ -870,15 +874,23 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
   cp.seg_cost = 0;
 
   if (plan.kind == 3) {
+    // bf16 caches: no plan launch, the attention kernel plans the call itself
+    // and writes a decode step's new rows. fp8 caches: the plan launch plans
+    // the call and quantizes the new rows first, which measured faster.
     const WsLayout lay = ws_layout(a.num_seqs, a.num_q_heads, 1, grid);
-    if ((e = launch_plan(a, grid, 1, 128, kDecodeSegmentCost, ws, stream)) != cudaSuccess) return e;
+    DecodeArgs at = a;
+    if (a.fp8) {
+      if ((e = launch_plan(a, grid, 1, 128, kDecodeSegmentCost, ws, stream)) != cudaSuccess) return e;
+      at.key_new = at.value_new = nullptr;
+    }
     cp.wph = 1;
     cp.seg_cost = kDecodeSegmentCost;
     cp.ml = reinterpret_cast<float2 *>(ws + lay.ml);
     cp.po = reinterpret_cast<float *>(ws + lay.o);
-    if ((e = launch_decode_tcg(a, grid, reinterpret_cast<float2 *>(ws + lay.ml),
-                               reinterpret_cast<float *>(ws + lay.o), kDecodeSegmentCost, stream)) !=
-        cudaSuccess)
+    if ((e = launch_decode_tcg(at, grid, reinterpret_cast<float2 *>(ws + lay.ml),
+                               reinterpret_cast<float *>(ws + lay.o), kDecodeSegmentCost,
+                               reinterpret_cast<int *>(ws + lay.total), tcg_cu_stride(a.num_seqs),
+                               stream)) != cudaSuccess)
       return e;
     // mixed batch: the prefill runs on the SMs the attention kernel leaves as
     // its CTAs finish; the combine below waits for the prefill, which waits

@@ -108,6 +108,25 @@ struct GParams {
   const float *k_scales;  // fp8 caches: [NB * bs, Hkv] row scales
   const float *v_scales;
   int seg_cost;           // units in front of each non-empty sequence in the flat space
+  // the plan: with bf16 caches computed by every CTA from the lengths and
+  // their bound, the prefix sums going to the workspace's cu[] (CTA 0; the
+  // combine reads them) or cu_copies + (b - 1) * cu_stride (CTA b > 0); with
+  // fp8 caches (which measured faster so) read from the workspace, where the
+  // plan launch before this kernel left it
+  const int32_t *context_lens;
+  int max_context_len;
+  int *cu_copies;
+  int cu_stride;
+  // decode step over bf16 caches (key_new == nullptr otherwise): each
+  // sequence's newest K/V row, [S, Hkv, 128] bf16 with these token strides in
+  // elements, is written to the cache by the CTA that owns the sequence's last
+  // position, before that stage is loaded
+  const __nv_bfloat16 *key_new;
+  const __nv_bfloat16 *value_new;
+  int64_t key_stride;
+  int64_t value_stride;
+  uint8_t *k_cache;
+  uint8_t *v_cache;
 };
 
 // shared-memory map, all offsets from a 1024-aligned base
@@ -382,8 +401,9 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // launched as a programmatic dependent of the plan kernel: let the combine
-  // pass behind this kernel be scheduled early too (it waits for this grid)
+  // launched as a programmatic dependent of the previous kernel on the stream:
+  // let the combine pass behind this kernel be scheduled early too (it waits
+  // for this grid)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const uint32_t bar0 = base + L.bar;
@@ -451,12 +471,72 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // everything above overlapped the plan kernel; its outputs (ranges, prefix
-  // sums, the decode step's new tokens) are read only after this wait
+  // everything above may overlap the previous kernel on the stream (launched
+  // as its programmatic dependent); the inputs are read only after this wait
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int total = reinterpret_cast<const int *>(p.ws)[0];
-  const int range = reinterpret_cast<const int *>(p.ws)[1];
-  const int *cu = reinterpret_cast<const int *>(p.ws + 256);
+  // The plan, computed by every CTA: prefix sums cu of the clamped lengths in
+  // the flat space (a non-empty sequence takes seg_cost units, then its
+  // tokens), the total, and the range size W = ceil(total / grid) rounded up
+  // to 16, at least 128. CTA 0 also leaves cu and (total, W) in the workspace
+  // for the combine.
+  constexpr bool kSelfPlan = !F8;
+  int *cu_w = (blockIdx.x == 0 || !kSelfPlan)
+                  ? reinterpret_cast<int *>(const_cast<uint8_t *>(p.ws) + 256)
+                  : p.cu_copies + static_cast<size_t>(blockIdx.x - 1) * p.cu_stride;
+  int total = 0;
+  int range = 0;
+  if (!kSelfPlan) {
+    total = reinterpret_cast<const int *>(p.ws)[0];
+    range = reinterpret_cast<const int *>(p.ws)[1];
+  } else {
+    int *wsum = reinterpret_cast<int *>(alpha_buf);  // scratch until the roles start
+    constexpr int kWarps = NT / 32;
+    for (int start = 0; start < p.num_seqs; start += NT) {
+      const int i = start + static_cast<int>(threadIdx.x);
+      int x = 0;
+      if (i < p.num_seqs) {
+        x = p.context_lens[i];
+        if (x < 0 || x > p.max_context_len) {
+          if (blockIdx.x == 0) raise_error(p.err, PKV_DEVERR_LENGTH);
+          x = x < 0 ? 0 : p.max_context_len;
+        }
+      }
+      int v = x > 0 ? x + p.seg_cost : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += y;
+      }
+      if (lane == 31) wsum[warp] = v;
+      __syncthreads();
+      if (warp == 0) {
+        int w = lane < kWarps ? wsum[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, w, off);
+          if (lane >= off) w += y;
+        }
+        if (lane < kWarps) wsum[lane] = w;
+      }
+      __syncthreads();
+      if (i < p.num_seqs) cu_w[i + 1] = total + v + (warp > 0 ? wsum[warp - 1] : 0);
+      total += wsum[kWarps - 1];
+      __syncthreads();
+    }
+    long long range_ll = (static_cast<long long>(total) + gridDim.x - 1) / gridDim.x;
+    range_ll = (range_ll + 15) / 16 * 16;
+    range = static_cast<int>(range_ll < 128 ? 128 : range_ll);
+    if (threadIdx.x == 0) {
+      cu_w[0] = 0;
+      if (blockIdx.x == 0) {
+        int *hdr = reinterpret_cast<int *>(const_cast<uint8_t *>(p.ws));
+        hdr[0] = total;
+        hdr[1] = range;
+      }
+    }
+    __syncthreads();  // the producers read cu_w
+  }
+  const int *cu = kSelfPlan ? cu_w : reinterpret_cast<const int *>(p.ws + 256);
   const int lo = static_cast<int>(blockIdx.x) * range;
   const int hi = min(lo + range, total);
   const uint32_t tmem_o = tmem;                       // O^T: columns [0, N)
@@ -559,6 +639,19 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         d.slot = complete ? -1 : (c0 <= lo ? 2 * int(blockIdx.x) : 2 * int(blockIdx.x) + 1);
         d.qbuf = 0;  // one Q^T buffer: refilled once the previous segment's S MMAs are done
         d.pad = 0;
+        // decode step (bf16 caches): if this CTA owns the sequence's last
+        // position, its new row (the K warp the K row, the V warp the V row) is
+        // loaded now, so the loads are done by the segment's last stage, where
+        // it is written. (fp8 caches: the rows are quantized by a launch before
+        // this kernel, which is faster than quantizing here.)
+        const bool owns_new = !F8 && p.key_new != nullptr && c1 <= hi;
+        uint4 nv[64 / T];   // this lane's 16-byte pieces of the row (Hkv * 256 B)
+        if (owns_new) {
+          const __nv_bfloat16 *src = (is_k ? p.key_new : p.value_new) +
+                                     static_cast<int64_t>(i) * (is_k ? p.key_stride : p.value_stride);
+#pragma unroll
+          for (int u = 0; u < 64 / T; ++u) nv[u] = reinterpret_cast<const uint4 *>(src)[u * 32 + lane];
+        }
         const int32_t *row = p.block_tables + static_cast<size_t>(i) * p.max_blocks_per_seq;
         int cached = -(1 << 30), my_id = -1;
         bool first = true;
@@ -577,6 +670,16 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           }
           d.pa = pa;
           d.flags = (first ? kFirst : 0) | (pa + T >= d.p1 ? kLast : 0);
+          if (owns_new && pa + T >= d.p1 && blk_row >= 0) {
+            // the sequence's last position is in this stage: write the new
+            // row there first, then let the copy engine read it
+            const int64_t slot = blk_row + (c1 - c0 - 1 - pa);
+            uint4 *d4 = reinterpret_cast<uint4 *>(is_k ? p.k_cache : p.v_cache) + slot * (16 * (128 / T));
+#pragma unroll
+            for (int u = 0; u < 64 / T; ++u) d4[u * 32 + lane] = nv[u];
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __syncwarp();
+          }
           ok = stage(d, blk_row, first);
           first = false;
         }
@@ -1176,7 +1279,7 @@ bool decode_tcg_supported(int num_q_heads, int num_kv_heads, int block_size, boo
 }
 
 cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *po, int seg_cost,
-                              cudaStream_t stream) {
+                              int *cu_copies, int cu_stride, cudaStream_t stream) {
   const int n_cols = (a.num_q_heads + 15) / 16 * 16;
   const bool f8 = a.fp8;
   const int stages = pick_stages(n_cols, f8);
@@ -1227,12 +1330,23 @@ cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *
   p.k_scales = a.k_scales;
   p.v_scales = a.v_scales;
   p.seg_cost = seg_cost;
+  p.context_lens = a.context_lens;
+  p.max_context_len = a.max_context_len;
+  p.cu_copies = cu_copies;
+  p.cu_stride = cu_stride;
+  p.key_new = static_cast<const __nv_bfloat16 *>(a.key_new);
+  p.value_new = static_cast<const __nv_bfloat16 *>(a.value_new);
+  p.key_stride = a.key_stride;
+  p.value_stride = a.value_stride;
+  p.k_cache = static_cast<uint8_t *>(const_cast<void *>(a.k_cache));
+  p.v_cache = static_cast<uint8_t *>(const_cast<void *>(a.v_cache));
   auto kern = tcg_kernel_for(T, p.group, f8);
   if (kern == nullptr) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the prologue (barriers, TMEM, descriptor
-  // prefetch) runs while the plan kernel finishes
+  // prefetch) runs while the previous kernel on the stream (the plan launch
+  // with fp8 caches) finishes
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(f8 ? kThreadsF8 : kThreads);

@@ -107,10 +107,15 @@ bool decode_tcg_supported(int num_q_heads, int num_kv_heads, int block_size, boo
 // (386 -> 378 us) and near best for 8 x 32768 + 248 x 200 (230 -> 206 us).
 constexpr int kDecodeSegmentCost = 64;
 
-// seg_cost: extra units the plan put in front of each non-empty sequence's
-// tokens in the flat space the CTA ranges cut (decode.cu, launch_paged_decode)
+// seg_cost: extra units in front of each non-empty sequence's tokens in the
+// flat space the CTA ranges cut. The kernel plans the call itself (every CTA
+// computes the prefix sums; CTA 0 leaves them in the workspace for the
+// combine, the others in cu_copies, cu_stride ints apart) and writes a decode
+// step's new rows (decode.cu, launch_paged_decode).
 cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *po, int seg_cost,
-                              cudaStream_t stream);
+                              int *cu_copies, int cu_stride, cudaStream_t stream);
+// ints between the per-CTA prefix-sum copies of the tcgen05 decode kernel
+inline int tcg_cu_stride(int num_seqs) { return (num_seqs + 1 + 63) / 64 * 64; }
 
 // tcgen05 decode kernel, one KV head per CTA range (decode_tc.cu)
 bool decode_tc_supported(int num_q_heads, int num_kv_heads, int block_size);
