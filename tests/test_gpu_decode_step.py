@@ -23,8 +23,9 @@ def run_step(w, t, m):
     return out
 
 
-# (Hkv, G, bs) covering the all-heads tcgen05 kernel, the per-head tcgen05
-# kernel and the CUDA-core kernel behind the step's planning launch
+# (Hkv, G, bs) covering the all-heads tcgen05 kernel (which plans the call and
+# writes the new rows itself), the per-head tcgen05 kernel and the CUDA-core
+# kernel (behind the step's planning launch)
 SHAPES = [(8, 4, 16), (8, 4, 256), (4, 8, 32), (16, 2, 16), (8, 1, 16), (2, 4, 16),
           (3, 5, 32), (8, 4, 3), (4, 2, 1)]
 
@@ -130,3 +131,51 @@ def test_decode_step_replays_from_a_cuda_graph_at_a_padded_batch():
         assert pkv.get_device_errors() == 0
         assert_close(out[:live], ref, f"graph step {k}")
         assert (out[live:] == 0).all()
+
+
+def test_decode_step_on_all_heads_kernel_reports_bad_metadata_and_skips_it():
+    """The all-heads kernel plans the call itself: a length beyond max_context_len
+    is clamped and reported, and a new row whose block id is out of range is not
+    written anywhere (and reported); the other sequences are still correct."""
+    lens = [40, 40, 300, 17]
+    w = W.decode_workload("step_bad_meta", lens, 32, 8, 16, seed=77)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    m = device_meta(w)
+    kn, vn = per_sequence_rows(w, t)
+    # sequence 1's last block id out of range: its new row must not be written
+    bt = m["block_tables"].clone()
+    bt[1, (lens[1] - 1) // 16] = w.num_blocks + 5
+    kc0, vc0 = t["k_cache"].clone(), t["v_cache"].clone()
+    pkv.decode_step(t["q"], kn, vn, t["k_cache"], t["v_cache"], bt, m["context_lens"], w.scale)
+    assert pkv.get_device_errors() & pkv._lib.DEVERR_BLOCK_ID
+    # every cache row other than the three good sequences' new rows is unchanged
+    slots = [int(w.slot_mapping[k]) for k in (0, 2, 3)]
+    flat0, flat = kc0.view(-1, 8, 128), t["k_cache"].view(-1, 8, 128)
+    mask = torch.ones(flat.shape[0], dtype=torch.bool, device="cuda")
+    mask[torch.tensor(slots, device="cuda")] = False
+    assert torch.equal(flat[mask], flat0[mask])
+    assert torch.equal(t["v_cache"].view(-1, 8, 128)[mask], vc0.view(-1, 8, 128)[mask])
+    # a length beyond the bound: clamped and reported
+    lens_t = m["context_lens"].clone()
+    lens_t[2] = 10_000
+    pkv.decode_step(t["q"], kn, vn, t["k_cache"], t["v_cache"], m["block_tables"], lens_t, w.scale,
+                    max_context_len=512)
+    assert pkv.get_device_errors() & pkv._lib.DEVERR_LENGTH
+
+
+def test_decode_step_on_all_heads_kernel_with_empty_and_many_sequences():
+    """Thousands of sequences (the per-CTA plan takes several passes over the
+    lengths), a fifth of them empty, on the all-heads kernel: every non-empty
+    sequence matches the oracle and every empty one gives a zero row."""
+    rng = np.random.default_rng(91)
+    lens = rng.integers(1, 60, size=2500)
+    lens[rng.choice(2500, 500, replace=False)] = 0
+    w = W.decode_workload("step_many", lens, 32, 8, 16, seed=92)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    m = device_meta(w)
+    ids = np.arange(w.num_seqs)
+    ref = decode_step_reference(w, ids, t["k_cache"], t["v_cache"], t["q"], t["key"], t["value"])
+    out = run_step(w, t, m)
+    assert_close(out, ref, w.name)
+    for i in np.nonzero(w.context_lens == 0)[0]:
+        assert (out[int(i)] == 0).all()
