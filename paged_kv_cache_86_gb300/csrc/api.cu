@@ -19,7 +19,50 @@ std::mutex g_mu;
 uint32_t *g_err_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 
+// The share of the SMs a mixed round gives to the prefill launch that runs
+// beside its decode kernel: kMixedSideGain times the prefill's share of an
+// estimate of the round's work -- with equal key counts per query row, decode
+// moves Hkv * 512 bytes per sequence and key at ~45 GB/s per SM, and prefill
+// does Hq * 512 flops per chunk row and key at ~8.5 TFLOP/s per SM -- capped at
+// kMixedSideMax. The estimate undercounts the prefill's share (the decode kernel
+// keeps most of its bandwidth on fewer SMs, and the prefill launch after the
+// decode kernel takes what is left), hence the gain, set by measurement.
+constexpr float kMixedSideGain = 1.6f;
+constexpr float kMixedSideMax = 0.45f;
+
+float mixed_side_share(int num_decode, int64_t chunk_rows, int num_q_heads, int num_kv_heads) {
+  const double dec = double(num_decode) * num_kv_heads * 512.0 / 45e9;
+  const double pre = double(chunk_rows) * num_q_heads * 512.0 / 8.5e12;
+  if (dec + pre <= 0.0) return 0.f;
+  const double share = kMixedSideGain * pre / (dec + pre);
+  return static_cast<float>(share < kMixedSideMax ? share : kMixedSideMax);
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A second stream per device on which a mixed round runs part of its prefill
+// beside the decode kernel, forked from and joined back into the caller's
+// stream by two events. Created on first use; the fork-launch-join sequence
+// is issued under g_side_mu so that concurrent callers do not interleave their
+// event records.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[kMaxDevices];
+
+cudaError_t side_stream_locked(int dev, SideStream **out) {
+  SideStream &s = g_side[dev];
+  if (s.stream == nullptr) {
+    cudaError_t e = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+  }
+  *out = &s;
+  return cudaSuccess;
+}
 
 pkv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
@@ -381,6 +424,33 @@ pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void 
                                 static_cast<int32_t>(row), key_token_stride, value_token_stride,
                                 int64_t(num_blocks) * block_size, err, st);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
+  // With the prefill interleaved, part of it also runs beside the decode: a
+  // launch on a share of the SMs (mixed_side_share) on the side stream, while
+  // the decode kernel takes the others; the launch between the decode kernel
+  // and its combine then takes the items left (both claim items from one ticket).
+  // The side launch may start first: its CTA count, not the stream order,
+  // keeps the decode kernel's SMs free.
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+  const int sms = pkv::sm_count(dev);
+  const int side_ctas =
+      interleave ? static_cast<int>(sms * mixed_side_share(num_decode_seqs, total_q - num_decode_seqs,
+                                                           num_q_heads, num_kv_heads))
+                 : 0;
+  std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
+  SideStream *side = nullptr;
+  if (side_ctas > 0) {
+    side_lock.lock();
+    if ((e = side_stream_locked(dev, &side)) != cudaSuccess) return PKV_ERR_CUDA;
+    pkv::PrefillArgs ps = pa;
+    ps.overlap_previous = false;
+    ps.max_ctas = side_ctas;
+    if ((e = cudaEventRecord(side->fork, st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(side->stream, side->fork, 0)) != cudaSuccess ||
+        (e = pkv::launch_paged_prefill(ps, side->stream)) != cudaSuccess ||
+        (e = cudaEventRecord(side->join, side->stream)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
   // 2. the decode sequences 0..D-1 (one query row each, rows 0..D-1)
   if (num_decode_seqs > 0) {
     int32_t *lens = static_cast<int32_t *>(workspace);
@@ -406,8 +476,11 @@ pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void 
     a.workspace_bytes = dec_bytes;
     a.err = err;
     a.interleave = interleave ? &pa : nullptr;
+    a.grid_override = side_ctas > 0 ? sms - side_ctas : 0;
     if ((e = pkv::launch_paged_decode(a, plan, st)) != cudaSuccess) return PKV_ERR_CUDA;
   }
+  if (side != nullptr && (e = cudaStreamWaitEvent(st, side->join, 0)) != cudaSuccess)
+    return PKV_ERR_CUDA;
   // 3. the prefill chunks, unless they ran between the decode kernels
   if (num_prefill > 0 && !interleave &&
       (e = pkv::launch_paged_prefill(pa, st)) != cudaSuccess)

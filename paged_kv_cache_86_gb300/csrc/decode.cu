@@ -856,7 +856,8 @@ size_t decode_workspace_upper_bound(int num_seqs, int num_q_heads, int num_kv_he
 
 cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
-  const int grid = plan.grid;
+  const int grid = (plan.kind == 3 && a.grid_override > 0 && a.grid_override < plan.grid)
+                       ? a.grid_override : plan.grid;
   const int wph = kConsumerWarps / a.num_kv_heads;
   const int group = a.num_q_heads / a.num_kv_heads;
   uint8_t *ws = static_cast<uint8_t *>(a.workspace);

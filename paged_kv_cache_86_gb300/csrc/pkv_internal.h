@@ -66,6 +66,9 @@ struct DecodeArgs {
   // the combine, so that it fills the SMs the attention kernel's tail leaves
   // (nullptr otherwise)
   const struct PrefillArgs *interleave = nullptr;
+  // all-heads tcgen05 kernel: CTAs to launch instead of one per SM (0: one per
+  // SM), leaving the other SMs to a kernel that runs beside it
+  int grid_override = 0;
   // fp8 E4M3 caches (uint8 codes) with fp32 row scales [NB * bs, Hkv]
   bool fp8 = false;
   const float *k_scales = nullptr;
@@ -154,6 +157,9 @@ struct PrefillArgs {
   // nothing that kernel writes. The kernel still waits for it before it
   // exits, so a later dependent sees both finished.
   bool overlap_previous = false;
+  // CTAs of the persistent kernel (0: one per SM); items are claimed from the
+  // work ticket, so two launches sharing one ticket split the items between them
+  int max_ctas = 0;
 };
 
 constexpr size_t kPrefillWorkspace = 256;

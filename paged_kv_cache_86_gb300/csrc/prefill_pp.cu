@@ -705,7 +705,9 @@ cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int sms = sm_count(dev);
   if (sms <= 0) return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
+  long long ctas = n_items < sms ? n_items : sms;
+  if (a.max_ctas > 0 && a.max_ctas < ctas) ctas = a.max_ctas;
+  const dim3 grid(static_cast<unsigned>(ctas));
   if (!a.overlap_previous) {
     prefill_pp_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();

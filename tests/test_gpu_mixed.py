@@ -91,3 +91,56 @@ def test_mixed_step_full_size_decode_rows_and_chunk_tiles():
     assert pkv.get_device_errors() == 0
     sel = np.sort(rows)
     assert_close(out[torch.from_numpy(sel).cuda()], ref[sel], w.name)
+
+
+def test_mixed_step_with_side_prefill_replays_from_a_cuda_graph():
+    """A round whose prefill also runs beside the decode kernel on the library's
+    second stream (forked from and joined into the caller's stream): captured
+    in a CUDA graph and replayed, it gives the eager call's output bit for bit
+    (which items each prefill launch claims varies, their arithmetic does not),
+    and the eager call matches the oracle."""
+    rng = np.random.default_rng(21)
+    dec = np.clip(np.rint(np.exp(np.log(800) + rng.standard_normal(128))), 16, 4096).astype(int)
+    w, d = mixed_workload("mixed_graph", dec.tolist(), [512] * 4, rng.integers(0, 3585, 4).tolist(),
+                          32, 8, 16, seed=22)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    m = device_meta(w)
+    kc0, vc0 = t["k_cache"].clone(), t["v_cache"].clone()
+    mq, mk = int(w.q_lens.max()), int(w.context_lens.max())
+    ws = torch.empty(pkv.mixed_workspace_size(d, 32, 8), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(t["q"])
+
+    def call():
+        pkv.mixed_step(t["q"], t["key"], t["value"], m["slot_mapping"], t["k_cache"], t["v_cache"],
+                       m["cu_seqlens_q"], m["cu_seqlens_k"], m["block_tables"], d, w.scale, mq, mk,
+                       out=out, workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    mask = np.zeros(w.num_q_rows, np.uint8)
+    cu = w.cu_seqlens_q
+    rows = set(range(d))
+    for i in range(d, w.num_seqs):
+        for r0 in range(int(cu[i]), int(cu[i + 1]), 128):
+            rows |= {r0, min(r0 + 127, int(cu[i + 1]) - 1)}
+    rows = np.array(sorted(rows))
+    mask[rows] = 1
+    ref = prefill_step_reference(w, kc0, vc0, t["q"], t["key"], t["value"], row_mask=mask)
+    assert_close(eager[torch.from_numpy(rows).cuda()], ref[rows], w.name)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()                      # warm-up on the capture stream
+        torch.cuda.synchronize()
+        out.zero_()
+        with torch.cuda.graph(g, stream=s):
+            call()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert pkv.get_device_errors() == 0
