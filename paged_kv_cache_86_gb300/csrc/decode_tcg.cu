@@ -540,7 +540,10 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int lo = static_cast<int>(blockIdx.x) * range;
   const int hi = min(lo + range, total);
   const uint32_t tmem_o = tmem;                       // O^T: columns [0, N)
-  auto tmem_s = [&](int b) { return tmem + N * (1 + b); };  // S^T buffers
+  // S^T buffers; fp8: each 2N wide, the hi half of Q^T in columns [0, N) and
+  // the lo half in [N, 2N)
+  constexpr int kSWidth = F8 ? 2 : 1;
+  auto tmem_s = [&](int b) { return tmem + N * (1 + kSWidth * b); };
   auto fail = [&]() {
     *abort_flag = 1;
     raise_error(p.err, PKV_DEVERR_TIMEOUT);
@@ -708,7 +711,7 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       // S is E4M3 x E4M3 (kind::f8f6f4), PV f16 x f16: format field 0 means
       // E4M3 for the one and f16 for the other
       constexpr uint32_t kFmt = ~((1u << 7) | (1u << 10));
-      const uint32_t idesc_s = umma_idesc_bf16(kRows, N, false) & kFmt;
+      const uint32_t idesc_s = umma_idesc_bf16(kRows, 2 * N, false) & kFmt;
       const uint32_t idesc_pv = (umma_idesc_bf16(kHD, N, false) | (1u << 15)) & kFmt;  // A (V) MN-major
       bool ok = true;
       int pv_issued = 0, s_issued = 0;
@@ -749,12 +752,13 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         if (do_s) {
           tc_fence_after();
-          // S^T = K . (Q_hi + Q_lo)^T: 32 dims per step, the raw K codes
-          // against the hi row (steps 0-3), then against the lo row (4-7)
-          const uint64_t dkr = desc_k(base + L.kr + sj * kRawStage, 0, 0), dq = desc_k(sQ, 0, small);
+          // [S_hi | S_lo]^T = K . [Q_hi ; Q_lo]^T: the N hi rows and the N lo
+          // rows of the split Q^T buffer are one 2N-row operand, so each
+          // step (32 dims) reads the raw K codes once
+          const uint64_t dkr = desc_k(base + L.kr + sj * kRawStage, 0, 0), dq = desc_k(sQ, 0, 0);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_f8(tmem_s(bj), dkr + kstep(kk & 3, 0), dq + kstep(kk, small >> 4), idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            umma_f8(tmem_s(bj), dkr + kstep(kk, 0), dq + kstep(kk, 0), idesc_s, kk > 0 ? 1u : 0u);
           umma_commit(s_full(bj));
           first_of = (first_of & ~(1u << (j & 31))) | ((flags & kFirst) ? 1u << (j & 31) : 0u);
           ++s_issued;
@@ -974,21 +978,42 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int j = 0;; ++j) {
       const int s = j % S;
       const int buf = j & 1;
+      const uint32_t ring_parity = (j / S) & 1;
+      // A stage's inputs are usually all in place when the softmax warps get
+      // to it (the loaders run stages ahead, S(j) was issued as soon as S(j-2)
+      // had been read), and each shared-memory round trip costs hundreds of
+      // cycles while the copy engine, the converters and the tensor core
+      // stream through shared memory. So the barriers of S(j), PV(j-2) and
+      // (fp8) the raw V stage are probed together with the wait for the stage
+      // descriptor, and the descriptor and the row scales are read together;
+      // only a barrier that was not complete yet is waited on further below.
+      bool vr_ready = !F8 || mbar_test_wait(vr_full(s), ring_parity);
+      bool s_ready = mbar_test_wait(s_full(buf), (j >> 1) & 1);
+      bool pv_ready = j < 2 || mbar_test_wait(pv_done(buf), ((j - 2) >> 1) & 1);
       GDesc d = {0, 0, 0, 0, kEnd, 0, 0, 0};
-      float kscale = 1.f;
-      if (ok && !warp_wait(k_full(s), (j / S) & 1, abort_flag)) ok = false;
+      float kscale = 1.f, vscale = 1.f;
+      if (ok && !warp_wait(k_full(s), ring_parity, abort_flag)) ok = false;
+      vr_ready = __all_sync(0xffffffffu, vr_ready);
       if (ok) {
-        d = desc[s];
-        // fp8: this row's K scale sits in the raw stage, which the loader may
-        // refill once every softmax warp has arrived on k_empty (below)
-        if (F8 && !(d.flags & kEnd)) {
+        const int4 *dv = reinterpret_cast<const int4 *>(desc + s);
+        const int4 d0 = dv[0], d1 = dv[1];
+        d = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+        // fp8: the row scales sit in the raw stages, which the loaders may
+        // refill once every softmax warp has arrived on k_empty (below) and
+        // the PV MMA of this stage has completed. Read whatever the stage
+        // holds (an end stage loads nothing, and its values go unused).
+        if (F8) {
           kscale = reinterpret_cast<const float *>(smem + L.kr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
-          if (d.flags & kFirst) {
+          if (vr_ready)
+            vscale = reinterpret_cast<const float *>(smem + L.vr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
+          if ((d.flags & (kFirst | kEnd)) == kFirst) {
 #pragma unroll
             for (int g = 0; g < G; ++g) qinv[g] = reinterpret_cast<const float *>(smem + L.qs)[head * G + g];
           }
         }
       }
+      s_ready = __all_sync(0xffffffffu, s_ready);
+      pv_ready = __all_sync(0xffffffffu, pv_ready);
       const bool end = ok && (d.flags & kEnd);
       const bool work = ok && !end;
       const bool first = (d.flags & kFirst) != 0;
@@ -997,13 +1022,25 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const bool partial = d.pa < d.p0 || d.pa + T > d.p1;
       float sc[G];
       bool need = false;
-      if (work && !warp_wait(s_full(buf), (j >> 1) & 1, abort_flag)) ok = false;
+      if (work && !s_ready && !warp_wait(s_full(buf), (j >> 1) & 1, abort_flag)) ok = false;
       if (ok && work) {
         tc_fence_after();
-        // the S^T columns of all heads of this warp in one load; keep this row's G
+        // the S^T columns of all heads of this warp in one load (fp8: one
+        // from each half, summed); keep this row's G
         float cols[kCols];
         tmem_ld_cols<kCols>(tmem_s(buf) + lane_off + warp_head0 * G, cols);
-        tmem_wait_ld();
+        if constexpr (F8) {
+          float lo[kCols];
+          tmem_ld_cols<kCols>(tmem_s(buf) + lane_off + N + warp_head0 * G, lo);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < kCols; ++i) {
+            asm volatile("" : "+f"(cols[i]), "+f"(lo[i]));  // the sums stay behind the wait
+            cols[i] += lo[i];
+          }
+        } else {
+          tmem_wait_ld();
+        }
         tc_fence_before();
         __syncwarp();
         // S^T[j & 1] has been read (S(j + 2) may overwrite it); S(j) has
@@ -1039,19 +1076,21 @@ decode_tcg_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       // PV(j-2) read this stage's P^T buffer: it must be done before the rewrite
       if (ok && work && j >= 2) {
-        if (warp_wait(pv_done(buf), ((j - 2) >> 1) & 1, abort_flag)) tc_fence_after();
+        if (pv_ready || warp_wait(pv_done(buf), ((j - 2) >> 1) & 1, abort_flag)) tc_fence_after();
         else ok = false;
       }
-      // fp8: P^T rows carry the V row scale, read from the raw V stage as soon
-      // as it has landed; a partial stage zeroes its masked rows of the
-      // converted V stage, so it waits for the conversion
-      if (ok && work && (F8 || partial) &&
-          !warp_wait((F8 && !partial) ? vr_full(s) : v_full(s), (j / S) & 1, abort_flag))
-        ok = false;
-      // issued here so that the load overlaps the barrier below
-      float vscale = 1.f;
-      if (F8 && ok && work)
-        vscale = reinterpret_cast<const float *>(smem + L.vr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
+      // a partial stage zeroes its masked rows of the converted V stage, so it
+      // waits for the conversion (fp8) or the load (bf16)
+      if (ok && work && partial && !warp_wait(v_full(s), ring_parity, abort_flag)) ok = false;
+      // fp8: P^T rows carry the V row scale, read from the raw V stage once it
+      // has landed (above, if it had by then; a partial stage's conversion
+      // implies it)
+      if (F8 && ok && work && !vr_ready) {
+        if (partial || warp_wait(vr_full(s), ring_parity, abort_flag))
+          vscale = reinterpret_cast<const float *>(smem + L.vr + s * kRawStage + kRawCodes)[t * p.num_kv_heads + head];
+        else
+          ok = false;
+      }
       if (!ok && lane == 0) {
         *stop_flag = 1;
         *abort_flag = 1;  // the other roles give up their waits too
@@ -1273,7 +1312,8 @@ bool decode_tcg_supported(int num_q_heads, int num_kv_heads, int block_size, boo
   if (num_q_heads % num_kv_heads != 0) return false;
   if (tcg_kernel_for(kRows / num_kv_heads, num_q_heads / num_kv_heads, fp8) == nullptr) return false;
   const int n_cols = (num_q_heads + 15) / 16 * 16;
-  if (n_cols > kMaxN) return false;
+  // O^T + the S^T buffers in TMEM
+  if (n_cols > kMaxN || (fp8 ? 5 : 3) * n_cols + 16 > 512) return false;
   const int T = kRows / num_kv_heads;
   return block_size % T == 0 && pick_stages(n_cols, fp8) > 0;
 }
@@ -1307,7 +1347,7 @@ cudaError_t launch_decode_tcg(const DecodeArgs &a, int grid, float2 *ml, float *
           : encode(&tk, a.k_cache, cd, cs, cb) && encode(&tv, a.v_cache, cd, cs, cb));
   if (!maps_ok) return cudaErrorInvalidValue;
   int tmem_cols = 32;
-  while (tmem_cols < 3 * n_cols + 16) tmem_cols <<= 1;
+  while (tmem_cols < (f8 ? 5 : 3) * n_cols + 16) tmem_cols <<= 1;
   GParams p;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.block_tables = a.block_tables;
