@@ -940,11 +940,11 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
   }
   const int warps = a.num_seqs * a.num_q_heads;
   const unsigned ctas = static_cast<unsigned>((warps + kCombineWarps - 1) / kCombineWarps);
-  if (plan.kind != 3) {
+  if (plan.kind == 1) {
     decode_combine_kernel<<<ctas, kCombineWarps * 32, 0, stream>>>(cp);
     return cudaGetLastError();
   }
-  // behind the all-heads tcgen05 kernel: a programmatic dependent launch hides
+  // behind a tcgen05 attention kernel: a programmatic dependent launch hides
   // the launch latency (the kernel waits for the attention grid first)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);

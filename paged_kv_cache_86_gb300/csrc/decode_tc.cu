@@ -156,11 +156,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const TcHeader hdr = *reinterpret_cast<const TcHeader *>(p.ws);
-  const int *cu = reinterpret_cast<const int *>(p.ws + 256);
-  const long long units = static_cast<long long>(hdr.total) * p.num_kv_heads;
-  const long long lo = static_cast<long long>(blockIdx.x) * hdr.range;
-  const long long hi = min(lo + hdr.range, units);
+  // launched as a programmatic dependent of the plan launch: let the combine
+  // behind this kernel be scheduled early too (it waits for this grid)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const uint32_t bar0 = base + kOffBar;
   auto kv_full = [&](int s) { return bar0 + 8u * s; };
@@ -207,6 +205,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // everything above may overlap the plan launch; the plan and the inputs
+  // are read only after this wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const TcHeader hdr = *reinterpret_cast<const TcHeader *>(p.ws);
+  const int *cu = reinterpret_cast<const int *>(p.ws + 256);
+  const long long units = static_cast<long long>(hdr.total) * p.num_kv_heads;
+  const long long lo = static_cast<long long>(blockIdx.x) * hdr.range;
+  const long long hi = min(lo + hdr.range, units);
   auto fail = [&]() {
     *abort_flag = 1;
     raise_error(p.err, PKV_DEVERR_TIMEOUT);
@@ -613,8 +619,19 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, int grid, float2 *ml, float *p
   p.ml = ml;
   p.po = po;
   p.err = a.err;
-  decode_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the set-up (barriers, TMEM) runs while the
+  // plan launch before it on the stream finishes
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel, tq, tk, tv, p);
 }
 
 }  // namespace pkv
