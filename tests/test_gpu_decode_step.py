@@ -74,11 +74,14 @@ def test_decode_step_512seq_full_size_every_sequence():
     assert torch.equal(flat_k[slots], t["key"]) and torch.equal(flat_v[slots], t["value"])
 
 
-def test_decode_step_replays_from_a_cuda_graph_at_a_padded_batch():
+@pytest.mark.parametrize("hkv,group", [(8, 4), (2, 4)])
+def test_decode_step_replays_from_a_cuda_graph_at_a_padded_batch(hkv, group):
     """37 live sequences padded to a captured batch of 64 with empty rows; the
     graph is replayed for three consecutive steps (context_lens grows by one
-    and new q / K / V rows arrive each step, all through the same buffers)."""
-    live, padded, hkv, group, bs = 37, 64, 8, 4, 16
+    and new q / K / V rows arrive each step, all through the same buffers).
+    Eight KV heads run the all-heads kernel, two the per-head kernel (its
+    launches chained as programmatic dependents inside the graph)."""
+    live, padded, bs = 37, 64, 16
     rng = np.random.default_rng(9)
     lens0 = (rng.integers(0, 40, size=live) * bs + rng.integers(1, bs - 3, size=live)).astype(np.int32)
     grown = np.concatenate([lens0 + 3, np.zeros(padded - live, np.int32)])  # blocks for 3 steps
