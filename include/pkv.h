@@ -369,9 +369,11 @@ pkv_status pkv_paged_decode_static_ws(void *out, const void *q,
  *                     256-byte aligned: the work ticket of the persistent
  *                     kernel, reset by the call itself; two calls in flight at
  *                     once need two workspaces.
- *   Supported: head_dim 128; num_q_heads a multiple of num_kv_heads;
- *   block_size a multiple of 8; num_seqs and ceil(max_seqlen_q / 128) at most
- *   65535. Unsupported shapes return PKV_ERR_SHAPE.
+ *   Supported: head_dim 128; num_q_heads a multiple of num_kv_heads; any
+ *   block_size >= 1 (K/V tiles of a block size that is a multiple of 8 are
+ *   loaded as TMA boxes, others are gathered row by row); num_seqs and
+ *   ceil(max_seqlen_q / 128) at most 65535. Unsupported shapes return
+ *   PKV_ERR_SHAPE.
  */
 size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t total_q,
                                   int32_t num_q_heads, int32_t head_dim);

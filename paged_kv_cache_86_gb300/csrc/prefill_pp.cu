@@ -86,12 +86,28 @@ struct PPParams {
   int max_seqlen_k;
   int causal;
   int box_rows;
+  // block sizes that are not a multiple of 8: the loaders gather K/V rows with
+  // cp.async (a TMA box must fill whole 8-row swizzle atoms)
+  const uint8_t *k_cache;
+  const uint8_t *v_cache;
+  int num_kv_heads;
   int q_tiles;       // 128-row query tiles of the longest chunk
   int pair_tiles;    // odd GQA group: A and B are two consecutive query tiles of one head
   uint32_t *ticket;  // next unclaimed work item (zeroed before the launch)
   float scale_log2;
   uint32_t *err;
 };
+
+// 16 bytes global -> shared, asynchronously; src_bytes 0 zero-fills them
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -147,6 +163,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const v
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
+// kGather: the loaders gather K/V rows with cp.async (block sizes that are not
+// a multiple of 8) instead of loading TMA boxes; a separate instance, so that
+// the box path compiles as if the gather did not exist
+template <bool kGather>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const PPParams p) {
@@ -346,48 +366,110 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           }
         }
         const int32_t *bt = p.block_tables + static_cast<size_t>(it.seq) * p.max_blocks_per_seq;
-        for (int j = 0; ok && j < it.n_tiles; ++j) {
-          const int s = issued % stages;
-          const int round = issued / stages;
-          int row = oob_row;
-          if (lane < pieces) {
-            const int key = j * kTile + lane * R;
-            if (key < it.k_len) {
-              const int blk = __ldg(bt + key / p.block_size);
-              if (blk >= 0 && blk < p.num_blocks) row = blk * p.block_size + key % p.block_size;
-              else if (is_k) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
-            }
-          }
-          const uint32_t full = is_k ? k_full(s) : v_full(s);
-          const uint32_t empty = is_k ? k_empty(s) : v_empty(s);
-          const uint32_t dst = is_k ? sK(s) : sV(s);
-          const CUtensorMap *map = is_k ? &tm_k : &tm_v;
-          int good = 1;
-          if (lane == 0) {
-            if (round > 0 && !mbar_wait(empty, (round - 1) & 1, abort_flag)) {
+        if constexpr (kGather) {
+          // Gather: the tile's 128 key rows (256 bytes each, one KV head) in
+          // 16-byte pieces, a half-warp per row, into the 128-byte-swizzled
+          // layout the TMA boxes produce; keys past k_len (or with a bad block
+          // id) are zero-filled. cp.async writes through the generic proxy, so
+          // a tile's full barrier is raised once its copies have landed and a
+          // proxy fence has ordered them before the tensor core's reads: the
+          // previous tile's after this tile's copies are issued, the item's
+          // last tile at the item's end.
+          const uint8_t *cache = is_k ? p.k_cache : p.v_cache;
+          const int half = lane >> 4, c = lane & 15;  // piece c: dims 8c .. 8c+7
+          for (int j = 0; ok && j < it.n_tiles; ++j) {
+            const int s = issued % stages;
+            const int round = issued / stages;
+            int good = 1;
+            if (lane == 0 && round > 0 && !mbar_wait(is_k ? k_empty(s) : v_empty(s), (round - 1) & 1,
+                                                     abort_flag)) {
               good = 0;
               fail();
-            } else {
-              mbar_arrive_expect_tx(full, kTileBytes);
             }
+            if (!__shfl_sync(0xffffffffu, good, 0)) {
+              ok = false;
+              break;
+            }
+            const uint32_t dst = is_k ? sK(s) : sV(s);
+#pragma unroll 1
+            for (int u = 0; u < kTile / 32; ++u) {
+              // cache row of key 32u + lane of the tile, -1 for none
+              int my_row = -1;
+              const int key_l = j * kTile + 32 * u + lane;
+              if (key_l < it.k_len) {
+                const int blk = __ldg(bt + key_l / p.block_size);
+                if (blk >= 0 && blk < p.num_blocks) my_row = blk * p.block_size + key_l % p.block_size;
+                else if (is_k) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+              }
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {  // keys 32u + 2i (lanes 0-15) and 32u + 2i + 1 (16-31)
+                const int kk = 2 * i + half;
+                const int row = __shfl_sync(0xffffffffu, my_row, kk);
+                const int key = 32 * u + kk;
+                const size_t src_row = static_cast<size_t>(row < 0 ? 0 : row) * p.num_kv_heads + it.kvh;
+                cp_async16(dst + (c >> 3) * kRegion + key * 128 + ((((c & 7) ^ (key & 7))) << 4),
+                           cache + src_row * (kHD * 2) + c * 16, row < 0 ? 0 : 16);
+              }
+            }
+            cp_async_commit();
+            if (j > 0) {  // the previous tile's copies (all but the newest group) have landed
+              cp_async_wait<1>();
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(is_k ? k_full((issued - 1) % stages) : v_full((issued - 1) % stages));
+            }
+            ++issued;
           }
-          good = __shfl_sync(0xffffffffu, good, 0);
-          if (!good) {
-            ok = false;
-            break;
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (ok && it.n_tiles > 0 && lane == 0)
+            mbar_arrive(is_k ? k_full((issued - 1) % stages) : v_full((issued - 1) % stages));
+        } else {
+          for (int j = 0; ok && j < it.n_tiles; ++j) {
+            const int s = issued % stages;
+            const int round = issued / stages;
+            int row = oob_row;
+            if (lane < pieces) {
+              const int key = j * kTile + lane * R;
+              if (key < it.k_len) {
+                const int blk = __ldg(bt + key / p.block_size);
+                if (blk >= 0 && blk < p.num_blocks) row = blk * p.block_size + key % p.block_size;
+                else if (is_k) raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+              }
+            }
+            const uint32_t full = is_k ? k_full(s) : v_full(s);
+            const uint32_t empty = is_k ? k_empty(s) : v_empty(s);
+            const uint32_t dst = is_k ? sK(s) : sV(s);
+            const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+            int good = 1;
+            if (lane == 0) {
+              if (round > 0 && !mbar_wait(empty, (round - 1) & 1, abort_flag)) {
+                good = 0;
+                fail();
+              } else {
+                mbar_arrive_expect_tx(full, kTileBytes);
+              }
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) {
+              ok = false;
+              break;
+            }
+            if (lane < pieces) {
+              tma_load_3d(dst + lane * R * 128, map, 0, it.kvh, row, full);
+              tma_load_3d(dst + kRegion + lane * R * 128, map, 64, it.kvh, row, full);
+            }
+            ++issued;
           }
-          if (lane < pieces) {
-            tma_load_3d(dst + lane * R * 128, map, 0, it.kvh, row, full);
-            tma_load_3d(dst + kRegion + lane * R * 128, map, 64, it.kvh, row, full);
-          }
-          ++issued;
         }
         ++items;
       }
       if (lane == 0) {  // drain: the last copies must land before the CTA exits
         if (is_k && items > 0) mbar_wait(q_full, (items - 1) & 1, nullptr);
-        for (int j = max(0, issued - stages); j < issued; ++j)
-          mbar_wait(is_k ? k_full(j % stages) : v_full(j % stages), (j / stages) & 1, nullptr);
+        if constexpr (!kGather)  // (gathered rows have landed at each item's end)
+          for (int j = max(0, issued - stages); j < issued; ++j)
+            mbar_wait(is_k ? k_full(j % stages) : v_full(j % stages), (j / stages) & 1, nullptr);
       }
     } else if (warp == kWarpMma) {
       // ------------------------------------------------------------ MMA issuer
@@ -648,23 +730,26 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t heads,
 }  // namespace
 
 bool prefill_pp_supported(int num_q_heads, int num_kv_heads, int block_size) {
-  return num_kv_heads >= 1 && num_q_heads % num_kv_heads == 0 && block_size % 8 == 0;
+  return num_kv_heads >= 1 && num_q_heads % num_kv_heads == 0 && block_size >= 1;
 }
 
 cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kSmemBytes);
-    // setmaxnreg.inc waits until the registers it asks for are free; the split
-    // only adds up if the kernel was built with exactly kRegsLaunch per thread,
-    // so refuse to launch any other build rather than risk a wait that never ends.
-    cudaFuncAttributes fa;
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_pp_kernel);
-    if (attr_err == cudaSuccess && fa.numRegs != kRegsLaunch) attr_err = cudaErrorInvalidConfiguration;
+    for (auto kern : {prefill_pp_kernel<false>, prefill_pp_kernel<true>}) {
+      if (attr_err == cudaSuccess)
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      // setmaxnreg.inc waits until the registers it asks for are free; the split
+      // only adds up if the kernel was built with exactly kRegsLaunch per thread,
+      // so refuse to launch any other build rather than risk a wait that never ends.
+      cudaFuncAttributes fa;
+      if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, kern);
+      if (attr_err == cudaSuccess && fa.numRegs != kRegsLaunch) attr_err = cudaErrorInvalidConfiguration;
+    }
   });
   if (attr_err != cudaSuccess) return attr_err;
+  auto kern = (a.block_size % 8 != 0) ? prefill_pp_kernel<true> : prefill_pp_kernel<false>;
   int box_rows = a.block_size & -a.block_size;
   if (box_rows > kTile) box_rows = kTile;
   CUtensorMap tq, tk, tv;
@@ -689,6 +774,9 @@ cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
   p.max_seqlen_k = a.max_seqlen_k;
   p.causal = a.causal ? 1 : 0;
   p.box_rows = box_rows;
+  p.k_cache = static_cast<const uint8_t *>(a.k_cache);
+  p.v_cache = static_cast<const uint8_t *>(a.v_cache);
+  p.num_kv_heads = a.num_kv_heads;
   p.scale_log2 = a.scale * kLog2e;
   p.err = a.err;
   p.q_tiles = (a.max_seqlen_q + kTile - 1) / kTile;
@@ -709,7 +797,7 @@ cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
   if (a.max_ctas > 0 && a.max_ctas < ctas) ctas = a.max_ctas;
   const dim3 grid(static_cast<unsigned>(ctas));
   if (!a.overlap_previous) {
-    prefill_pp_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -722,7 +810,7 @@ cudaError_t launch_prefill_pp(const PrefillArgs &a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_pp_kernel, tq, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
 }
 
 }  // namespace pkv

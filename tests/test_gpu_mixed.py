@@ -28,7 +28,8 @@ def run_mixed(w, d, t):
     return out, m
 
 
-@pytest.mark.parametrize("hkv,group,bs", [(8, 4, 16), (2, 4, 16), (8, 2, 32), (4, 3, 16)])
+@pytest.mark.parametrize("hkv,group,bs", [(8, 4, 16), (2, 4, 16), (8, 2, 32), (4, 3, 16), (8, 4, 1),
+                                          (2, 2, 4)])
 def test_mixed_step_matches_the_oracle(hkv, group, bs):
     w, d = mixed_workload(f"mixed_{hkv}x{group}_bs{bs}", [1, 2, 17, 300, 1000], [3, 130, 64],
                           [0, 70, 500], hkv * group, hkv, bs, seed=400 + hkv + group + bs)

@@ -51,9 +51,26 @@ def test_prefill_varlen(q_lens, prefixes):
     check(W.prefill_workload("p_varlen", q_lens, prefixes, 32, 8, 16, seed=sum(q_lens)))
 
 
-@pytest.mark.parametrize("bs", [8, 16, 24, 32, 128, 256])
+@pytest.mark.parametrize("bs", [1, 2, 4, 8, 12, 16, 20, 24, 32, 128, 256])
 def test_prefill_block_sizes(bs):
+    # block sizes that are not a multiple of 8 gather K/V rows with cp.async
+    # instead of TMA boxes; ragged last tiles in both chunks
     check(W.prefill_workload(f"p_bs{bs}", [130, 77], [300, 45], 16, 8, bs, seed=300 + bs))
+
+
+@pytest.mark.parametrize("hkv,group,bs", [(3, 3, 1), (8, 4, 1), (2, 8, 4), (1, 4, 6)])
+def test_prefill_gathered_rows_with_head_groups(hkv, group, bs):
+    # the gather path with an odd group (paired query tiles), GQA groups up to
+    # 8 and a single KV head, chunks over several 128-key tiles
+    check(W.prefill_workload(f"p_gather_h{hkv}g{group}b{bs}", [300, 129, 40], [500, 0, 1000],
+                             hkv * group, hkv, bs, seed=700 + hkv * 10 + group + bs))
+
+
+def test_prefill_page_size_one_chunks_every_row():
+    # token-level paging (one token per block, shuffled over the pool), the
+    # shape of the benchmark's chunks at a smaller count
+    prefixes = np.random.default_rng(87001).integers(0, 1501, size=6)
+    check(W.prefill_workload("p_page1", [512] * 6, prefixes, 32, 8, 1, seed=87001))
 
 
 @pytest.mark.parametrize("hkv,group", [(3, 3), (2, 5), (4, 1), (1, 3)])
