@@ -329,6 +329,64 @@ decode_split_kernel(const SplitParams p) {
       return good != 0;
     };
 
+    // Blocks shorter than a stage: one stage takes ntok consecutive tokens of
+    // the sequence over several blocks, lane t copying token t's K and V rows
+    // (and token t + 32's when a stage holds more than 32 tokens) to stage
+    // row t. A block id out of range skips the whole stage.
+    auto issue_rows = [&](int seq, int pos, int ntok, int flags, int slot, const int32_t *row) {
+      const int s = issued % kStages;
+      const uint32_t round = static_cast<uint32_t>(issued / kStages);
+      int blk[2] = {0, 0};
+      bool bad = false;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int t = lane + 32 * u;
+        if (t < ntok) {
+          blk[u] = __ldg(row + (pos + t) / p.block_size);
+          bad |= blk[u] < 0 || blk[u] >= p.num_blocks;
+        }
+      }
+      bad = __any_sync(kFull, bad);
+      const uint32_t fb = smem_addr(&full_bar[s]);
+      int good = 1;
+      if (lane == 0) {
+        if (round > 0 && !mbar_wait(smem_addr(&empty_bar[s]), (round - 1) & 1, abort_flag)) {
+          good = 0;
+          *abort_flag = 1;
+          raise_error(p.err, PKV_DEVERR_TIMEOUT);
+        } else {
+          if (bad) {
+            flags |= kSkip;
+            raise_error(p.err, PKV_DEVERR_BLOCK_ID);
+          }
+          StageDesc d;
+          d.seq = seq; d.pos = pos; d.ntok = ntok; d.flags = flags; d.slot = slot;
+          d.pad0 = d.pad1 = d.pad2 = 0;
+          desc[s] = d;
+          if (bad) mbar_arrive(fb);
+          else mbar_arrive_expect_tx(fb, static_cast<uint32_t>(2 * ntok * row_bytes));
+        }
+      }
+      good = __shfl_sync(kFull, good, 0);  // (also orders lane 0's expect_tx before the copies)
+      if (good && !bad) {
+        const uint64_t policy_rows = l2_policy_evict_first();
+        const uint32_t dst0 = smem_addr(stage_base + s * kStageBytes);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int t = lane + 32 * u;
+          if (t < ntok) {
+            const size_t src = (static_cast<size_t>(blk[u]) * p.block_size + (pos + t) % p.block_size) *
+                               row_bytes;
+            const uint32_t dst = dst0 + t * row_bytes;
+            bulk_g2s(dst, p.k_cache + src, row_bytes, fb, policy_rows);
+            bulk_g2s(dst + kStageBytes / 2, p.v_cache + src, row_bytes, fb, policy_rows);
+          }
+        }
+      }
+      if (good) ++issued;
+      return good != 0;
+    };
+
     if (lo < hi) {
       // first sequence whose tokens reach past lo
       int a = 0, b = p.num_seqs - 1;
@@ -347,7 +405,14 @@ decode_split_kernel(const SplitParams p) {
         const int32_t *row = p.block_tables + static_cast<size_t>(i) * p.max_blocks_per_seq;
         int cached = -1 << 30, my_id = -1;
         bool first = true;
-        for (int pos = seg_lo; ok && pos < seg_hi;) {
+        for (int pos = seg_lo; ok && pos < seg_hi && p.block_size < stage_tokens;) {
+          const int ntok = min(stage_tokens, seg_hi - pos);
+          const int flags = (first ? kFirst : 0) | (pos + ntok == seg_hi ? kLast : 0);
+          first = false;
+          ok = issue_rows(i, pos, ntok, flags, slot, row);
+          pos += ntok;
+        }
+        for (int pos = seg_lo; ok && pos < seg_hi && p.block_size >= stage_tokens;) {
           const int lb = pos / p.block_size;
           const int off = pos - lb * p.block_size;
           const int ntok = min(min(stage_tokens, p.block_size - off), seg_hi - pos);
@@ -812,17 +877,23 @@ bool choose_decode_plan(int num_q_heads, int num_kv_heads, int block_size, Decod
     plan->grid = decode_tc_grid();
     return plan->grid > 0;
   }
-  if (decode_tc_supported(num_q_heads, num_kv_heads, block_size)) {
+  // the CUDA-core kernel spreads 8 consumer warps evenly over the KV heads and
+  // is instantiated for groups of 1, 2, 4 and 8 query heads
+  const int group = num_q_heads / num_kv_heads;
+  const bool split_ok =
+      kConsumerWarps % num_kv_heads == 0 && (group == 1 || group == 2 || group == 4 || group == 8);
+  // The per-head tcgen05 kernel loads block-sized TMA boxes: from 16 rows up it
+  // is the faster one, at 8-row boxes the CUDA-core kernel, whose stages take
+  // whole token rows over several blocks, measured faster (512 sequences,
+  // 8 KV heads, block 8: 0.51 against 0.71 ms; 4 KV heads: 0.24 against 0.37)
+  if (decode_tc_supported(num_q_heads, num_kv_heads, block_size) &&
+      (block_size % 16 == 0 || !split_ok)) {
     plan->kind = 2;
     plan->tc = true;
     plan->grid = decode_tc_grid();
     return plan->grid > 0;
   }
-  // the CUDA-core kernel spreads 8 consumer warps evenly over the KV heads and
-  // is instantiated for groups of 1, 2, 4 and 8 query heads
-  const int group = num_q_heads / num_kv_heads;
-  if (kConsumerWarps % num_kv_heads != 0 || (group != 1 && group != 2 && group != 4 && group != 8))
-    return false;
+  if (!split_ok) return false;
   plan->kind = 1;
   plan->tc = false;
   plan->grid = split_grid(num_q_heads, num_kv_heads, status);

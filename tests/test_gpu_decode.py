@@ -60,7 +60,8 @@ def test_decode_head_configurations(hkv, group):
 def test_decode_more_head_shapes(hkv, group, bs):
     # all-heads tcgen05 kernel when Hkv is a power of two >= 4 and 128/Hkv divides
     # the block size; per-head tcgen05 kernel for other block sizes that are
-    # multiples of 8; the CUDA-core split kernel for the rest
+    # multiples of 16 (of 8 when the CUDA-core kernel cannot take the heads:
+    # 1 x 12 at block 8); the CUDA-core split kernel for the rest
     lens = [1, 9, 128, 129, 700, 2000]
     w = W.decode_workload(f"shape_{hkv}x{group}_bs{bs}", lens, hkv * group, hkv, bs,
                           seed=500 + hkv * 31 + group * 7 + bs)
