@@ -372,9 +372,10 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           // layout the TMA boxes produce; keys past k_len (or with a bad block
           // id) are zero-filled. cp.async writes through the generic proxy, so
           // a tile's full barrier is raised once its copies have landed and a
-          // proxy fence has ordered them before the tensor core's reads: the
-          // previous tile's after this tile's copies are issued, the item's
-          // last tile at the item's end.
+          // proxy fence has ordered them before the tensor core's reads. The
+          // warp waits for that before it moves on: the ring's depth, not this
+          // warp, keeps copies ahead of the MMAs (raising a tile only after the
+          // next one was issued made each PV wait for the one before it).
           const uint8_t *cache = is_k ? p.k_cache : p.v_cache;
           const int half = lane >> 4, c = lane & 15;  // piece c: dims 8c .. 8c+7
           for (int j = 0; ok && j < it.n_tiles; ++j) {
@@ -412,19 +413,12 @@ prefill_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               }
             }
             cp_async_commit();
-            if (j > 0) {  // the previous tile's copies (all but the newest group) have landed
-              cp_async_wait<1>();
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(is_k ? k_full((issued - 1) % stages) : v_full((issued - 1) % stages));
-            }
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(is_k ? k_full(s) : v_full(s));
             ++issued;
           }
-          cp_async_wait<0>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (ok && it.n_tiles > 0 && lane == 0)
-            mbar_arrive(is_k ? k_full((issued - 1) % stages) : v_full((issued - 1) % stages));
         } else {
           for (int j = 0; ok && j < it.n_tiles; ++j) {
             const int s = issued % stages;
