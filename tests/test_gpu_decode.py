@@ -56,12 +56,15 @@ def test_decode_head_configurations(hkv, group):
 
 @pytest.mark.parametrize("hkv,group,bs", [(16, 1, 16), (3, 5, 32), (2, 16, 16), (1, 12, 8),
                                            (8, 4, 12), (4, 4, 6), (4, 4, 32), (32, 2, 16),
-                                           (8, 3, 16), (16, 8, 16), (64, 1, 16)])
+                                           (8, 3, 16), (16, 8, 16), (64, 1, 16), (2, 4, 3),
+                                           (1, 2, 8), (2, 8, 1), (1, 1, 5)])
 def test_decode_more_head_shapes(hkv, group, bs):
-    # all-heads tcgen05 kernel when Hkv is a power of two >= 4 and 128/Hkv divides
-    # the block size; per-head tcgen05 kernel for other block sizes that are
-    # multiples of 16 (of 8 when the CUDA-core kernel cannot take the heads:
-    # 1 x 12 at block 8); the CUDA-core split kernel for the rest
+    # all-heads tcgen05 kernel when Hkv is 4, 8 or 16, G is 1, 2, 4 or 8 and
+    # 128/Hkv divides the block size; per-head tcgen05 kernel for other block
+    # sizes that are multiples of 16 (of 8 when the CUDA-core kernel cannot
+    # take the heads: 1 x 12 at 8); the CUDA-core split kernel for the rest
+    # (8 x 4 at 12, 4 x 4 at 6, 2 x 4 at 3, 1 x 2 at 8, 2 x 8 at 1, 1 x 1 at 5;
+    # at blocks shorter than a stage its stages span several blocks)
     lens = [1, 9, 128, 129, 700, 2000]
     w = W.decode_workload(f"shape_{hkv}x{group}_bs{bs}", lens, hkv * group, hkv, bs,
                           seed=500 + hkv * 31 + group * 7 + bs)

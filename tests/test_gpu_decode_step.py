@@ -25,9 +25,9 @@ def run_step(w, t, m):
 
 # (Hkv, G, bs) covering the all-heads tcgen05 kernel (which plans the call and
 # writes the new rows itself), the per-head tcgen05 kernel and the CUDA-core
-# kernel (behind the step's planning launch)
+# kernel (behind the step's planning launch; blocks 3, 1 and 5)
 SHAPES = [(8, 4, 16), (8, 4, 256), (4, 8, 32), (16, 2, 16), (8, 1, 16), (2, 4, 16),
-          (3, 5, 32), (8, 4, 3), (4, 2, 1)]
+          (3, 5, 32), (8, 4, 3), (4, 2, 1), (2, 2, 5)]
 
 
 @pytest.mark.parametrize("hkv,group,bs", SHAPES)
