@@ -47,7 +47,7 @@ def oracle_step_fp8(w, seq_ids, kc, vc, ks, vs, t):
 
 
 @pytest.mark.parametrize("hkv,group,bs", [(8, 4, 16), (8, 1, 16), (8, 2, 32), (4, 8, 32),
-                                          (4, 2, 64), (8, 2, 256)])
+                                          (4, 2, 64), (8, 2, 256), (8, 8, 16)])
 def test_fp8_store_and_decode_match_the_oracle(hkv, group, bs):
     lens = [1, 2, 15, 16, 17, 0, 300, 1025, 77, 2000]
     w = W.decode_workload(f"fp8_{hkv}x{group}_bs{bs}", lens, hkv * group, hkv, bs,
@@ -130,7 +130,8 @@ def run_step_fp8(w, t, kc, vc, ks, vs):
     return out
 
 
-@pytest.mark.parametrize("hkv,group,bs", [(8, 4, 16), (8, 1, 16), (4, 8, 32), (8, 2, 256)])
+@pytest.mark.parametrize("hkv,group,bs", [(8, 4, 16), (8, 1, 16), (4, 8, 32), (8, 2, 256),
+                                          (8, 8, 32)])
 def test_fp8_decode_step_matches_the_oracle(hkv, group, bs):
     lens = [1, 2, 16, 17, 0, 300, 1023, 5, 129, 2000, 0, 64]
     w = W.decode_workload(f"fp8_step_{hkv}x{group}_bs{bs}", lens, hkv * group, hkv, bs,
