@@ -131,8 +131,14 @@ pkv_status pkv_store_kvcache(const void *key, const void *value,
  * The result equals pkv_store_kvcache followed by pkv_paged_prefill over the
  * whole batch; the decode sequences run on the split decode kernels instead of
  * occupying a 128-row query tile each. A decode sequence with other than one
- * query row sets PKV_DEVERR_LENGTH. Launches: store, decode (plan, attention,
- * combine), prefill, in stream order.
+ * query row sets PKV_DEVERR_LENGTH. Launches: the store, then the decode
+ * (attention, combine) and the chunks' prefill. With the all-heads decode
+ * kernel, part of the prefill runs beside it on a second stream of the
+ * library (created on first use), forked from and joined back to `stream` by
+ * events within the call, so work queued on `stream` afterwards follows all
+ * of it and a CUDA graph captures the fork and the join; the rest of the
+ * prefill takes the SMs the decode kernel frees. Otherwise the launches run
+ * in stream order.
  */
 size_t pkv_mixed_workspace_size(int32_t num_decode_seqs, int32_t num_q_heads,
                                 int32_t num_kv_heads, int32_t head_dim);
