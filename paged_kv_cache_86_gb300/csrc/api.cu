@@ -340,6 +340,20 @@ size_t pkv_mixed_workspace_size(int32_t num_decode_seqs, int32_t num_q_heads,
   return dec == 0 ? 0 : lens + dec + pkv::kPrefillWorkspace;
 }
 
+namespace {
+// The persistent prefill kernel numbers its work items (a 128-row query tile
+// of two heads, or two tiles of one head for an odd GQA group, per sequence)
+// in 32 bits; shapes with more items than that are refused.
+bool prefill_items_fit(int32_t max_seqlen_q, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t num_seqs) {
+  const int64_t q_tiles = (int64_t(max_seqlen_q) + 127) / 128;
+  const bool pair_tiles = (num_q_heads / num_kv_heads) % 2 != 0;
+  const int64_t items = pair_tiles ? (q_tiles + 1) / 2 * num_q_heads * int64_t(num_seqs)
+                                   : q_tiles * (num_q_heads / 2) * int64_t(num_seqs);
+  return items < (int64_t(1) << 31);
+}
+}  // namespace
+
 pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void *value,
                           const int32_t *slot_mapping, int64_t key_token_stride,
                           int64_t value_token_stride, void *k_cache, void *v_cache,
@@ -360,6 +374,8 @@ pkv_status pkv_mixed_step(void *out, const void *q, const void *key, const void 
   if (int64_t(max_seqlen_k) > int64_t(max_blocks_per_seq) * block_size) return PKV_ERR_ARG;
   if (total_q < num_decode_seqs || num_seqs - num_decode_seqs > 65535) return PKV_ERR_ARG;
   if ((int64_t(max_seqlen_q) + 127) / 128 > 65535) return PKV_ERR_ARG;
+  if (!prefill_items_fit(max_seqlen_q, num_q_heads, num_kv_heads, num_seqs - num_decode_seqs))
+    return PKV_ERR_ARG;
   if (num_seqs == 0 || total_q == 0) return PKV_OK;
   if (!out || !q || !key || !value || !slot_mapping || !k_cache || !v_cache || !cu_seqlens_q ||
       !cu_seqlens_k || !block_tables || !workspace)
@@ -515,6 +531,7 @@ pkv_status pkv_paged_prefill(void *out, const void *q, const void *k_cache, cons
   if (!pkv::prefill_supported(num_q_heads, num_kv_heads, block_size)) return PKV_ERR_SHAPE;
   if (num_seqs > 65535 || num_q_heads > 65535) return PKV_ERR_ARG;  // grid y / z limits
   if ((int64_t(max_seqlen_q) + 127) / 128 > 65535) return PKV_ERR_ARG;
+  if (!prefill_items_fit(max_seqlen_q, num_q_heads, num_kv_heads, num_seqs)) return PKV_ERR_ARG;
   if (num_seqs == 0 || total_q == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_tables)
     return PKV_ERR_ARG;

@@ -69,6 +69,11 @@ def test_host_validation_needs_no_gpu(lib):
                                  float("nan"), null, 0, 0, null) == -1
     assert lib.pkv_paged_prefill(null, null, null, null, null, null, 8, 8, null, 4, 1, 8, 8, 2,
                                  128, 16, 8, 0.1, 1, null, 0, 1, null) == -3
+    # 65535 chunks of up to 2048 query tiles, 32 head pairs: 2^32 work items,
+    # more than the prefill kernel can number (32 bits)
+    assert lib.pkv_paged_prefill(null, null, null, null, null, null, 2048 * 128, 2048 * 128, null,
+                                 16384, 65535, 1 << 30, 64, 8, 128, 16, 8, 0.1, 1, null, 0, 0,
+                                 null) == -1
 
 
 def test_decode_step_host_validation_needs_no_gpu(lib):
