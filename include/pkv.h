@@ -190,10 +190,13 @@ pkv_status pkv_store_kvcache_fp8(const void *key, const void *value,
  * of two and split into two E4M3 terms whose sum is the scaled row (exact for
  * bf16 q except for entries under about 2^-10 of the row's largest, off by at
  * most 2^-10 of the scaled unit there); V is expanded to f16 with its row
- * scales folded into the softmax weights. Supported: head_dim 128,
- * num_kv_heads 4 or 8, num_q_heads / num_kv_heads in {1, 2, 4, 8} (so
- * num_q_heads <= 64), block_size a multiple of 128 / num_kv_heads; other
- * shapes return PKV_ERR_SHAPE.
+ * scales folded into the softmax weights. That kernel takes num_kv_heads 4
+ * or 8 with block_size a multiple of 128 / num_kv_heads; other block sizes,
+ * and 1 or 2 KV heads, run on the CUDA-core kernel, which expands the codes
+ * to fp32 and applies the row scales to the scores and the weights.
+ * Supported: head_dim 128, num_kv_heads in {1, 2, 4, 8}, num_q_heads /
+ * num_kv_heads in {1, 2, 4, 8}, any block_size >= 1; other shapes return
+ * PKV_ERR_SHAPE.
  */
 pkv_status pkv_paged_decode_fp8(void *out, const void *q,
                                 const void *k_cache, const void *v_cache,

@@ -245,7 +245,26 @@ struct SplitParams {
   float2 *ml;    // partial (m, l) records
   float *po;     // partial normalised outputs
   uint32_t *err;
+  const float *k_scales;  // fp8 caches: [NB * bs, Hkv] row scales
+  const float *v_scales;
 };
+
+// A stage holds kConsumerWarps * kTokensPerWarp / Hkv tokens of all KV heads:
+// with fp8 caches their row scales (token-major, one per KV head) sit beside it
+constexpr int kScaleEntries = kConsumerWarps * kTokensPerWarp;
+
+// Two E4M3 codes (the first in the low byte) -> two floats, exactly.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t codes) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<unsigned short>(codes & 0xffffu)));
+  return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
 
 template <int G>
 struct GroupTraits {
@@ -253,7 +272,10 @@ struct GroupTraits {
   static constexpr int kScatterShift = 4 - kLogG;  // head of a lane after the reduce-scatter
 };
 
-template <int G>
+// F8: the caches hold E4M3 codes with a scale per (token, KV head) row; the
+// codes are expanded on the CUDA cores and the scales applied to the scores
+// (K) and to the softmax weights (V).
+template <int G, bool F8>
 __global__ void __launch_bounds__(kThreads, G <= 4 ? 2 : 1)
 decode_split_kernel(const SplitParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -262,7 +284,8 @@ decode_split_kernel(const SplitParams p) {
   uint64_t *empty_bar = full_bar + kStages;
   StageDesc *desc = reinterpret_cast<StageDesc *>(empty_bar + kStages);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(desc + kStages);
-  float *score_buf = reinterpret_cast<float *>(desc + kStages) + 32;
+  float *scale_buf = reinterpret_cast<float *>(desc + kStages) + 32;  // [stage][K, V][entry]
+  float *score_buf = scale_buf + kStages * 2 * kScaleEntries;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -270,7 +293,8 @@ decode_split_kernel(const SplitParams p) {
   const int *cu = reinterpret_cast<const int *>(p.ws + 256);
   const int lo = static_cast<int>(blockIdx.x) * hdr.range;
   const int hi = min(lo + hdr.range, hdr.total);
-  const int row_bytes = p.num_kv_heads * kHeadBytes;
+  constexpr int head_bytes = F8 ? kHeadDim : kHeadBytes;  // one token of one KV head
+  const int row_bytes = p.num_kv_heads * head_bytes;
   const int wph = kConsumerWarps / p.num_kv_heads;  // consumer warps per KV head
 
   if (threadIdx.x == 0) {
@@ -285,7 +309,8 @@ decode_split_kernel(const SplitParams p) {
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    const int stage_tokens = (kStageBytes / 2) / row_bytes;
+    // tokens a stage's consumer warps take (bf16: the whole K half of a stage)
+    const int stage_tokens = kScaleEntries / p.num_kv_heads;
     const uint64_t policy = l2_policy_evict_first();
     int issued = 0;
     bool ok = true;
@@ -296,12 +321,25 @@ decode_split_kernel(const SplitParams p) {
       const int s = issued % kStages;
       const uint32_t round = static_cast<uint32_t>(issued / kStages);
       int good = 1;
+      if (lane == 0 && round > 0 && !mbar_wait(smem_addr(&empty_bar[s]), (round - 1) & 1, abort_flag)) {
+        good = 0;
+        *abort_flag = 1;
+        raise_error(p.err, PKV_DEVERR_TIMEOUT);
+      }
+      if constexpr (F8) {  // the rows' scales, written before the stage is armed
+        good = __shfl_sync(kFull, good, 0);
+        if (good && (flags & kEnd) == 0 && blk >= 0 && blk < p.num_blocks) {
+          float *sk = scale_buf + s * 2 * kScaleEntries;
+          const int64_t r0 = (static_cast<int64_t>(blk) * p.block_size + off) * p.num_kv_heads;
+          for (int e = lane; e < ntok * p.num_kv_heads; e += 32) {
+            sk[e] = __ldg(p.k_scales + r0 + e);
+            sk[kScaleEntries + e] = __ldg(p.v_scales + r0 + e);
+          }
+        }
+        __syncwarp();
+      }
       if (lane == 0) {
-        if (round > 0 && !mbar_wait(smem_addr(&empty_bar[s]), (round - 1) & 1, abort_flag)) {
-          good = 0;
-          *abort_flag = 1;
-          raise_error(p.err, PKV_DEVERR_TIMEOUT);
-        } else {
+        if (good) {
           const bool valid = (flags & kEnd) == 0 && blk >= 0 && blk < p.num_blocks;
           if ((flags & kEnd) == 0 && !valid) {
             flags |= kSkip;
@@ -349,12 +387,29 @@ decode_split_kernel(const SplitParams p) {
       bad = __any_sync(kFull, bad);
       const uint32_t fb = smem_addr(&full_bar[s]);
       int good = 1;
+      if (lane == 0 && round > 0 && !mbar_wait(smem_addr(&empty_bar[s]), (round - 1) & 1, abort_flag)) {
+        good = 0;
+        *abort_flag = 1;
+        raise_error(p.err, PKV_DEVERR_TIMEOUT);
+      }
+      if constexpr (F8) {  // the rows' scales, written before the stage is armed
+        good = __shfl_sync(kFull, good, 0);
+        float *sk = scale_buf + s * 2 * kScaleEntries;
+        for (int e = lane; e < 2 * 32 && good && !bad; e += 32) {
+          // entry e: token e / Hkv (its block held by lane t & 31 in blk[t >> 5])
+          const int t = e / p.num_kv_heads;
+          const int b0 = __shfl_sync(kFull, blk[0], t & 31), b1 = __shfl_sync(kFull, blk[1], t & 31);
+          if (e < ntok * p.num_kv_heads) {
+            const int64_t rr = (static_cast<int64_t>(t < 32 ? b0 : b1) * p.block_size +
+                                (pos + t) % p.block_size) * p.num_kv_heads + e % p.num_kv_heads;
+            sk[e] = __ldg(p.k_scales + rr);
+            sk[kScaleEntries + e] = __ldg(p.v_scales + rr);
+          }
+        }
+        __syncwarp();
+      }
       if (lane == 0) {
-        if (round > 0 && !mbar_wait(smem_addr(&empty_bar[s]), (round - 1) & 1, abort_flag)) {
-          good = 0;
-          *abort_flag = 1;
-          raise_error(p.err, PKV_DEVERR_TIMEOUT);
-        } else {
+        if (good) {
           if (bad) {
             flags |= kSkip;
             raise_error(p.err, PKV_DEVERR_BLOCK_ID);
@@ -487,16 +542,29 @@ decode_split_kernel(const SplitParams p) {
     const int t0 = sub * kTokensPerWarp;
     const int nw = (d.flags & kSkip) ? 0 : min(max(d.ntok - t0, 0), kTokensPerWarp);
     if (nw > 0) {
+      // lane l16 of each half-warp holds dims 8 l16 .. 8 l16 + 7 of a row
       const uint32_t kb = smem_addr(stage_base + s * kStageBytes) + t0 * row_bytes +
-                          head * kHeadBytes + l16 * 16;
+                          head * head_bytes + l16 * (head_bytes / 16);
       const uint32_t vb = kb + kStageBytes / 2;
+      // fp8: row scales of this warp's tokens, entry (token, KV head)
+      const float *sks = scale_buf + s * 2 * kScaleEntries + t0 * p.num_kv_heads + head;
 
       // scores of this warp's tokens, two tokens (one per half-warp) at a time
       for (int it = 0; it < (nw + 1) >> 1; ++it) {
         const int j = 2 * it + hf;
-        const uint4 kr = lds128(kb + j * row_bytes);
-        const float2 k0 = bf16x2_to_float2(kr.x), k1 = bf16x2_to_float2(kr.y);
-        const float2 k2 = bf16x2_to_float2(kr.z), k3 = bf16x2_to_float2(kr.w);
+        float2 k0, k1, k2, k3;
+        if constexpr (F8) {
+          const uint2 kr = lds64(kb + j * row_bytes);
+          k0 = e4m3x2_to_float2(kr.x); k1 = e4m3x2_to_float2(kr.x >> 16);
+          k2 = e4m3x2_to_float2(kr.y); k3 = e4m3x2_to_float2(kr.y >> 16);
+        } else {
+          const uint4 kr = lds128(kb + j * row_bytes);
+          k0 = bf16x2_to_float2(kr.x); k1 = bf16x2_to_float2(kr.y);
+          k2 = bf16x2_to_float2(kr.z); k3 = bf16x2_to_float2(kr.w);
+        }
+        // (fp8: the K row's scale multiplies the dot product; j past nw reads
+        // an unused entry of the stage)
+        const float kscale = F8 ? sks[j * p.num_kv_heads] : 1.f;
         float sv[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -504,7 +572,7 @@ decode_split_kernel(const SplitParams p) {
           a2 = ffma2(q2[g][1], k1, a2);
           a2 = ffma2(q2[g][2], k2, a2);
           a2 = ffma2(q2[g][3], k3, a2);
-          sv[g] = a2.x + a2.y;
+          sv[g] = (a2.x + a2.y) * kscale;
         }
         // reduce-scatter over the 16 lanes of the half-warp: each level halves
         // the heads a lane keeps and adds its partner's copy of them
@@ -562,11 +630,19 @@ decode_split_kernel(const SplitParams p) {
       }
       __syncwarp();
 
-      // P * V
+      // P * V (fp8: the V row's scale multiplies the softmax weights)
       for (int j = hf; j < nw; j += 2) {
-        const uint4 vr = lds128(vb + j * row_bytes);
-        const float2 v0f = bf16x2_to_float2(vr.x), v1f = bf16x2_to_float2(vr.y);
-        const float2 v2f = bf16x2_to_float2(vr.z), v3f = bf16x2_to_float2(vr.w);
+        float2 v0f, v1f, v2f, v3f;
+        if constexpr (F8) {
+          const uint2 vr = lds64(vb + j * row_bytes);
+          v0f = e4m3x2_to_float2(vr.x); v1f = e4m3x2_to_float2(vr.x >> 16);
+          v2f = e4m3x2_to_float2(vr.y); v3f = e4m3x2_to_float2(vr.y >> 16);
+        } else {
+          const uint4 vr = lds128(vb + j * row_bytes);
+          v0f = bf16x2_to_float2(vr.x); v1f = bf16x2_to_float2(vr.y);
+          v2f = bf16x2_to_float2(vr.z); v3f = bf16x2_to_float2(vr.w);
+        }
+        const float vscale = F8 ? sks[kScaleEntries + j * p.num_kv_heads] : 1.f;
         float pj[G];
         if constexpr (G == 1) {
           pj[0] = sc[j];
@@ -582,7 +658,7 @@ decode_split_kernel(const SplitParams p) {
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float2 pp = make_float2(pj[g], pj[g]);
+          const float2 pp = make_float2(pj[g] * vscale, pj[g] * vscale);
           acc[g][0] = ffma2(pp, v0f, acc[g][0]);
           acc[g][1] = ffma2(pp, v1f, acc[g][1]);
           acc[g][2] = ffma2(pp, v2f, acc[g][2]);
@@ -765,16 +841,23 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
 size_t split_smem_bytes(int group) {
   return size_t(kStages) * kStageBytes + 2 * kStages * sizeof(uint64_t) +
          kStages * sizeof(StageDesc) + 32 * sizeof(float) +
+         size_t(kStages) * 2 * kScaleEntries * sizeof(float) +
          size_t(kConsumerWarps) * kTokensPerWarp * group * sizeof(float);
 }
 
+// both instances (bf16, fp8) of a group; the grid follows the bf16 one's
+// occupancy (the CTAs wait on none of each other, so more CTAs than fit at
+// once only queue)
 template <int G>
 cudaError_t prepare_split(int *ctas_per_sm) {
   const size_t smem = split_smem_bytes(G);
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G>,
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_split_kernel<G>,
+  e = cudaFuncSetAttribute(decode_split_kernel<G, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_split_kernel<G, false>,
                                                        kThreads, smem);
 }
 
@@ -864,14 +947,9 @@ size_t tc_workspace(int num_seqs, int group, int grid) {
 bool choose_decode_plan(int num_q_heads, int num_kv_heads, int block_size, DecodePlan *plan,
                         cudaError_t *status, bool fp8) {
   *status = cudaSuccess;
-  if (fp8) {  // quantized caches: the all-heads tcgen05 kernel only
-    if (!decode_tcg_supported(num_q_heads, num_kv_heads, block_size, true)) return false;
-    plan->kind = 3;
-    plan->tc = false;
-    plan->grid = decode_tc_grid();
-    return plan->grid > 0;
-  }
-  if (decode_tcg_supported(num_q_heads, num_kv_heads, block_size)) {
+  // fp8 caches: the all-heads tcgen05 kernel where its fp8 instance applies,
+  // else the CUDA-core kernel
+  if (decode_tcg_supported(num_q_heads, num_kv_heads, block_size, fp8)) {
     plan->kind = 3;
     plan->tc = false;
     plan->grid = decode_tc_grid();
@@ -886,7 +964,7 @@ bool choose_decode_plan(int num_q_heads, int num_kv_heads, int block_size, Decod
   // is the faster one, at 8-row boxes the CUDA-core kernel, whose stages take
   // whole token rows over several blocks, measured faster (512 sequences,
   // 8 KV heads, block 8: 0.51 against 0.71 ms; 4 KV heads: 0.24 against 0.37)
-  if (decode_tc_supported(num_q_heads, num_kv_heads, block_size) &&
+  if (!fp8 && decode_tc_supported(num_q_heads, num_kv_heads, block_size) &&
       (block_size % 16 == 0 || !split_ok)) {
     plan->kind = 2;
     plan->tc = true;
@@ -1001,11 +1079,22 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const DecodePlan &plan, cud
     cp.ml = sp.ml;
     cp.po = sp.po;
     const size_t smem = split_smem_bytes(group);
-    switch (group) {
-      case 1: decode_split_kernel<1><<<grid, kThreads, smem, stream>>>(sp); break;
-      case 2: decode_split_kernel<2><<<grid, kThreads, smem, stream>>>(sp); break;
-      case 4: decode_split_kernel<4><<<grid, kThreads, smem, stream>>>(sp); break;
-      default: decode_split_kernel<8><<<grid, kThreads, smem, stream>>>(sp); break;
+    sp.k_scales = a.k_scales;
+    sp.v_scales = a.v_scales;
+    if (a.fp8) {
+      switch (group) {
+        case 1: decode_split_kernel<1, true><<<grid, kThreads, smem, stream>>>(sp); break;
+        case 2: decode_split_kernel<2, true><<<grid, kThreads, smem, stream>>>(sp); break;
+        case 4: decode_split_kernel<4, true><<<grid, kThreads, smem, stream>>>(sp); break;
+        default: decode_split_kernel<8, true><<<grid, kThreads, smem, stream>>>(sp); break;
+      }
+    } else {
+      switch (group) {
+        case 1: decode_split_kernel<1, false><<<grid, kThreads, smem, stream>>>(sp); break;
+        case 2: decode_split_kernel<2, false><<<grid, kThreads, smem, stream>>>(sp); break;
+        case 4: decode_split_kernel<4, false><<<grid, kThreads, smem, stream>>>(sp); break;
+        default: decode_split_kernel<8, false><<<grid, kThreads, smem, stream>>>(sp); break;
+      }
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

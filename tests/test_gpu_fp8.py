@@ -46,8 +46,11 @@ def oracle_step_fp8(w, seq_ids, kc, vc, ks, vs, t):
     return out[np.asarray(seq_ids)], (k8, v8, k_s, v_s)
 
 
+# the all-heads tcgen05 kernel (Hkv 4 or 8, 128/Hkv dividing the block size),
+# else the CUDA-core kernel (2 x 4 at 16, 8 x 4 at 1, 1 x 8 at 4, 4 x 2 at 12)
 @pytest.mark.parametrize("hkv,group,bs", [(8, 4, 16), (8, 1, 16), (8, 2, 32), (4, 8, 32),
-                                          (4, 2, 64), (8, 2, 256), (8, 8, 16)])
+                                          (4, 2, 64), (8, 2, 256), (8, 8, 16), (2, 4, 16),
+                                          (8, 4, 1), (1, 8, 4), (4, 2, 12)])
 def test_fp8_store_and_decode_match_the_oracle(hkv, group, bs):
     lens = [1, 2, 15, 16, 17, 0, 300, 1025, 77, 2000]
     w = W.decode_workload(f"fp8_{hkv}x{group}_bs{bs}", lens, hkv * group, hkv, bs,
@@ -92,7 +95,7 @@ def test_fp8_decode_512seq_full_size_every_sequence():
 
 
 def test_fp8_decode_rejects_shapes_without_the_kernel():
-    w = W.decode_workload("fp8_bad", [5, 9], 6, 2, 16, seed=32)     # Hkv 2: no fp8 kernel
+    w = W.decode_workload("fp8_bad", [5, 9], 6, 2, 16, seed=32)     # 3 query heads per KV head: no fp8 kernel
     t = {k: v.cuda() for k, v in w.tensors.items()}
     kc, vc, ks, vs = fp8_case(w, 32)
     with pytest.raises(pkv.PkvError) as e:
@@ -131,7 +134,7 @@ def run_step_fp8(w, t, kc, vc, ks, vs):
 
 
 @pytest.mark.parametrize("hkv,group,bs", [(8, 4, 16), (8, 1, 16), (4, 8, 32), (8, 2, 256),
-                                          (8, 8, 32)])
+                                          (8, 8, 32), (2, 2, 5), (8, 4, 3)])
 def test_fp8_decode_step_matches_the_oracle(hkv, group, bs):
     lens = [1, 2, 16, 17, 0, 300, 1023, 5, 129, 2000, 0, 64]
     w = W.decode_workload(f"fp8_step_{hkv}x{group}_bs{bs}", lens, hkv * group, hkv, bs,
