@@ -59,7 +59,7 @@ def parse():
                     help="time only the chunked-prefill row (store + prefill), for profiling")
     ap.add_argument("--only-row", default=None,
                     choices=["fp8", "copy", "mixed", "store", "decode_3seq", "decode_64seq",
-                             "decode_longtail"],
+                             "decode_longtail", "small_blocks"],
                     help="time only one row (fp8 decode, block copy, mixed round, sustained "
                          "store, or another decode workload), for profiling (--num-seqs applies "
                          "to the fp8 row, --store-copies to the store row)")
@@ -884,6 +884,50 @@ def timed_after_clean_flush(fn, steps, device):
     return statistics.median(times)
 
 
+def measure_small_blocks(device, steps):
+    """Block sizes below a stage or tile (token-level paging among them): the
+    512-sequence decode (lognormal lengths, Hq 32 / Hkv 8; bf16 and fp8 E4M3)
+    and the 32 x 512 chunked prefill over the same prefixes as the prefill row,
+    at block sizes 16 (the reference), 8, 4 and 1; each call timed with CUDA
+    events after a clean L2 refill. Not part of the default run."""
+    import torch
+    import paged_kv_cache_86_gb300 as pkv
+    from paged_kv_cache_86_gb300 import workloads as W
+    res = {}
+    lens = W.lognormal_lengths(np.random.default_rng(86003 + 1000), 512)
+    for bs in (16, 8, 1):
+        w = W.decode_workload(f"decode_512seq_bs{bs}", lens, 32, 8, bs, 86003, pool="fragmented",
+                              fill="device", device=device)
+        t = {k: v.to(device) for k, v in w.tensors.items() if k in ("q", "k_cache", "v_cache")}
+        bt = torch.from_numpy(w.block_tables).to(device)
+        cl = torch.from_numpy(w.context_lens).to(device)
+        res[f"decode_512seq_bs{bs}_ms"] = timed_after_clean_flush(
+            lambda: pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], bt, cl, w.scale), steps, device)
+        del t
+        kc, ks = W.fp8_pool(w.num_blocks, w.block_size, w.num_kv_heads, 7, device=device)
+        vc, vs = W.fp8_pool(w.num_blocks, w.block_size, w.num_kv_heads, 8, device=device)
+        q = torch.randn(w.num_seqs, 32, 128, device=device).to(torch.bfloat16)
+        res[f"fp8_decode_512seq_bs{bs}_ms"] = timed_after_clean_flush(
+            lambda: pkv.paged_decode_fp8(q, kc, vc, ks, vs, bt, cl, w.scale), steps, device)
+        del kc, vc, ks, vs
+    prefixes = np.random.default_rng(86005 + 1000).integers(0, 3584 + 1, size=32)
+    for bs in (16, 8, 4, 1):
+        w = W.prefill_workload(f"prefill_32x512_bs{bs}", [512] * 32, prefixes, 32, 8, bs, 86005,
+                               fill="device", device=device)
+        t = {k: v.to(device) for k, v in w.tensors.items() if k in ("q", "k_cache", "v_cache")}
+        cq = torch.from_numpy(w.cu_seqlens_q).to(device)
+        ck = torch.from_numpy(w.cu_seqlens_k).to(device)
+        bt = torch.from_numpy(w.block_tables).to(device)
+        res[f"prefill_32x512_bs{bs}_ms"] = timed_after_clean_flush(
+            lambda: pkv.paged_prefill(t["q"], t["k_cache"], t["v_cache"], cq, ck, bt, w.scale,
+                                      max_seqlen_q=512, max_seqlen_k=int(w.context_lens.max())),
+            steps, device)
+        del t
+    res["kernels"] = ("decode: all-heads tcgen05 at 16, CUDA-core with stages over several blocks "
+                      "below; prefill: TMA boxes at 16 and 8, rows gathered with cp.async below 8")
+    return res
+
+
 def measure_prefill(args, device, steps):
     """The chunked-prefill row: store of 16384 chunk tokens, then causal paged
     prefill of 32 chunks of 512 over cached prefixes, each timed with CUDA events."""
@@ -1013,6 +1057,8 @@ def main():
             res = {"copy_blocks_row": measure_copy_blocks(device, steps)}
         elif args.only_row == "store":
             res = {"store_row": measure_store_sustained(device, copies=args.store_copies)}
+        elif args.only_row == "small_blocks":
+            res = {"small_blocks_row": measure_small_blocks(device, steps)}
         elif args.only_row.startswith("decode_"):
             res = {"decode_config_row": measure_decode_config(args.only_row, device, steps)}
         else:
