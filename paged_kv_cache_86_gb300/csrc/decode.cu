@@ -249,9 +249,13 @@ struct SplitParams {
   const float *v_scales;
 };
 
-// A stage holds kConsumerWarps * kTokensPerWarp / Hkv tokens of all KV heads:
-// with fp8 caches their row scales (token-major, one per KV head) sit beside it
-constexpr int kScaleEntries = kConsumerWarps * kTokensPerWarp;
+// A consumer warp takes kTokensPerWarp tokens of a stage (fp8 caches, whose
+// rows are half the bytes: twice as many), so a stage holds
+// kConsumerWarps * tokens-per-warp / Hkv tokens of all KV heads; with fp8 caches
+// their row scales (token-major, one per KV head) sit beside it. Shared memory
+// is laid out for the larger fp8 counts.
+constexpr int kTokensPerWarpMax = 2 * kTokensPerWarp;
+constexpr int kScaleEntriesMax = kConsumerWarps * kTokensPerWarpMax;
 
 // Two E4M3 codes (the first in the low byte) -> two floats, exactly.
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t codes) {
@@ -284,8 +288,11 @@ decode_split_kernel(const SplitParams p) {
   uint64_t *empty_bar = full_bar + kStages;
   StageDesc *desc = reinterpret_cast<StageDesc *>(empty_bar + kStages);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(desc + kStages);
+  constexpr int kTPW = F8 ? kTokensPerWarpMax : kTokensPerWarp;  // tokens per consumer warp
+  constexpr int kEntries = kConsumerWarps * kTPW;  // (token, KV head) entries of a stage
+  constexpr int kRowsPerLane = kEntries / 32;      // token rows a lane copies (one KV head)
   float *scale_buf = reinterpret_cast<float *>(desc + kStages) + 32;  // [stage][K, V][entry]
-  float *score_buf = scale_buf + kStages * 2 * kScaleEntries;
+  float *score_buf = scale_buf + kStages * 2 * kScaleEntriesMax;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -310,7 +317,7 @@ decode_split_kernel(const SplitParams p) {
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     // tokens a stage's consumer warps take (bf16: the whole K half of a stage)
-    const int stage_tokens = kScaleEntries / p.num_kv_heads;
+    const int stage_tokens = kEntries / p.num_kv_heads;
     const uint64_t policy = l2_policy_evict_first();
     int issued = 0;
     bool ok = true;
@@ -329,11 +336,11 @@ decode_split_kernel(const SplitParams p) {
       if constexpr (F8) {  // the rows' scales, written before the stage is armed
         good = __shfl_sync(kFull, good, 0);
         if (good && (flags & kEnd) == 0 && blk >= 0 && blk < p.num_blocks) {
-          float *sk = scale_buf + s * 2 * kScaleEntries;
+          float *sk = scale_buf + s * 2 * kEntries;
           const int64_t r0 = (static_cast<int64_t>(blk) * p.block_size + off) * p.num_kv_heads;
           for (int e = lane; e < ntok * p.num_kv_heads; e += 32) {
             sk[e] = __ldg(p.k_scales + r0 + e);
-            sk[kScaleEntries + e] = __ldg(p.v_scales + r0 + e);
+            sk[kEntries + e] = __ldg(p.v_scales + r0 + e);
           }
         }
         __syncwarp();
@@ -368,19 +375,23 @@ decode_split_kernel(const SplitParams p) {
     };
 
     // Blocks shorter than a stage: one stage takes ntok consecutive tokens of
-    // the sequence over several blocks, lane t copying token t's K and V rows
-    // (and token t + 32's when a stage holds more than 32 tokens) to stage
-    // row t. A block id out of range skips the whole stage.
+    // the sequence over several blocks. Lane c copies the run of the stage's
+    // tokens that lies in the c-th block it touches (and runs c + 32, ...
+    // when there are more than 32), K and V, as one copy each. A block id out
+    // of range skips the whole stage.
     auto issue_rows = [&](int seq, int pos, int ntok, int flags, int slot, const int32_t *row) {
       const int s = issued % kStages;
       const uint32_t round = static_cast<uint32_t>(issued / kStages);
-      int blk[2] = {0, 0};
+      const int lb0 = pos / p.block_size;
+      const int nruns = (pos + ntok - 1) / p.block_size - lb0 + 1;  // <= ntok
+      int blk[kRowsPerLane];
       bool bad = false;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int t = lane + 32 * u;
-        if (t < ntok) {
-          blk[u] = __ldg(row + (pos + t) / p.block_size);
+      for (int u = 0; u < kRowsPerLane; ++u) {
+        blk[u] = 0;
+        const int c = lane + 32 * u;
+        if (c < nruns) {
+          blk[u] = __ldg(row + lb0 + c);
           bad |= blk[u] < 0 || blk[u] >= p.num_blocks;
         }
       }
@@ -394,16 +405,22 @@ decode_split_kernel(const SplitParams p) {
       }
       if constexpr (F8) {  // the rows' scales, written before the stage is armed
         good = __shfl_sync(kFull, good, 0);
-        float *sk = scale_buf + s * 2 * kScaleEntries;
-        for (int e = lane; e < 2 * 32 && good && !bad; e += 32) {
-          // entry e: token e / Hkv (its block held by lane t & 31 in blk[t >> 5])
+        float *sk = scale_buf + s * 2 * kEntries;
+        for (int e = lane; e < kEntries && good && !bad; e += 32) {
+          // entry e: token e / Hkv, in run c (its block held by lane c & 31 in blk[c >> 5])
           const int t = e / p.num_kv_heads;
-          const int b0 = __shfl_sync(kFull, blk[0], t & 31), b1 = __shfl_sync(kFull, blk[1], t & 31);
+          const int c = (pos + t) / p.block_size - lb0;
+          int b = 0;
+#pragma unroll
+          for (int u = 0; u < kRowsPerLane; ++u) {
+            const int bu = __shfl_sync(kFull, blk[u], c & 31);
+            if ((c >> 5) == u) b = bu;
+          }
           if (e < ntok * p.num_kv_heads) {
-            const int64_t rr = (static_cast<int64_t>(t < 32 ? b0 : b1) * p.block_size +
-                                (pos + t) % p.block_size) * p.num_kv_heads + e % p.num_kv_heads;
+            const int64_t rr = (static_cast<int64_t>(b) * p.block_size + (pos + t) % p.block_size) *
+                                   p.num_kv_heads + e % p.num_kv_heads;
             sk[e] = __ldg(p.k_scales + rr);
-            sk[kScaleEntries + e] = __ldg(p.v_scales + rr);
+            sk[kEntries + e] = __ldg(p.v_scales + rr);
           }
         }
         __syncwarp();
@@ -427,14 +444,17 @@ decode_split_kernel(const SplitParams p) {
         const uint64_t policy_rows = l2_policy_evict_first();
         const uint32_t dst0 = smem_addr(stage_base + s * kStageBytes);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int t = lane + 32 * u;
-          if (t < ntok) {
-            const size_t src = (static_cast<size_t>(blk[u]) * p.block_size + (pos + t) % p.block_size) *
+        for (int u = 0; u < kRowsPerLane; ++u) {
+          const int c = lane + 32 * u;
+          if (c < nruns) {
+            const int a = max(pos, (lb0 + c) * p.block_size);            // first token of the run
+            const int e = min(pos + ntok, (lb0 + c + 1) * p.block_size);  // one past its last
+            const size_t src = (static_cast<size_t>(blk[u]) * p.block_size + a % p.block_size) *
                                row_bytes;
-            const uint32_t dst = dst0 + t * row_bytes;
-            bulk_g2s(dst, p.k_cache + src, row_bytes, fb, policy_rows);
-            bulk_g2s(dst + kStageBytes / 2, p.v_cache + src, row_bytes, fb, policy_rows);
+            const uint32_t dst = dst0 + (a - pos) * row_bytes;
+            const uint32_t bytes = static_cast<uint32_t>((e - a) * row_bytes);
+            bulk_g2s(dst, p.k_cache + src, bytes, fb, policy_rows);
+            bulk_g2s(dst + kStageBytes / 2, p.v_cache + src, bytes, fb, policy_rows);
           }
         }
       }
@@ -502,7 +522,7 @@ decode_split_kernel(const SplitParams p) {
   const int my_head_after_scatter = l16 >> Tr::kScatterShift;
   const bool score_writer = (l16 & ((16 / G) - 1)) == 0;
   const int own_g = lane & (G - 1);  // head whose score sum this lane keeps
-  float *sc = score_buf + warp * kTokensPerWarp * G;
+  float *sc = score_buf + warp * kTPW * G;
 
   float2 q2[G][4];
   float2 acc[G][4];
@@ -539,15 +559,15 @@ decode_split_kernel(const SplitParams p) {
       l_part = 0.f;
     }
 
-    const int t0 = sub * kTokensPerWarp;
-    const int nw = (d.flags & kSkip) ? 0 : min(max(d.ntok - t0, 0), kTokensPerWarp);
+    const int t0 = sub * kTPW;
+    const int nw = (d.flags & kSkip) ? 0 : min(max(d.ntok - t0, 0), kTPW);
     if (nw > 0) {
       // lane l16 of each half-warp holds dims 8 l16 .. 8 l16 + 7 of a row
       const uint32_t kb = smem_addr(stage_base + s * kStageBytes) + t0 * row_bytes +
                           head * head_bytes + l16 * (head_bytes / 16);
       const uint32_t vb = kb + kStageBytes / 2;
       // fp8: row scales of this warp's tokens, entry (token, KV head)
-      const float *sks = scale_buf + s * 2 * kScaleEntries + t0 * p.num_kv_heads + head;
+      const float *sks = scale_buf + s * 2 * kEntries + t0 * p.num_kv_heads + head;
 
       // scores of this warp's tokens, two tokens (one per half-warp) at a time
       for (int it = 0; it < (nw + 1) >> 1; ++it) {
@@ -593,11 +613,17 @@ decode_split_kernel(const SplitParams p) {
       }
       __syncwarp();
 
-      // online softmax update, once per stage: entry e = token * G + head
+      // online softmax update, once per stage: entry e = token * G + head, lane
+      // l holding entries l, l + 32, ... (all of head l % G)
+      constexpr int kVals = (kTPW * G + 31) / 32;
       const int ne = nw * G;
-      const float v0 = lane < ne ? sc[lane] : -INFINITY;
-      const float v1 = (G == 8 && lane + 32 < ne) ? sc[lane + 32] : -INFINITY;
-      float mx = fmaxf(v0, v1);
+      float vals[kVals];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < kVals; ++u) {
+        vals[u] = lane + 32 * u < ne ? sc[lane + 32 * u] : -INFINITY;
+        mx = fmaxf(mx, vals[u]);
+      }
 #pragma unroll
       for (int off = 16; off >= G; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
       float alpha[G];
@@ -615,11 +641,16 @@ decode_split_kernel(const SplitParams p) {
           alpha_own = alpha[g];
         }
       }
-      const float p0 = lane < ne ? fast_exp2(v0 - m_own) : 0.f;
-      const float p1 = (G == 8 && lane + 32 < ne) ? fast_exp2(v1 - m_own) : 0.f;
-      if (lane < ne) sc[lane] = p0;
-      if (G == 8 && lane + 32 < ne) sc[lane + 32] = p1;
-      l_part = l_part * alpha_own + p0 + p1;
+      float psum = 0.f;
+#pragma unroll
+      for (int u = 0; u < kVals; ++u) {
+        if (lane + 32 * u < ne) {
+          const float pu = fast_exp2(vals[u] - m_own);
+          sc[lane + 32 * u] = pu;
+          psum += pu;
+        }
+      }
+      l_part = l_part * alpha_own + psum;
       if (rescale) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -642,7 +673,7 @@ decode_split_kernel(const SplitParams p) {
           v0f = bf16x2_to_float2(vr.x); v1f = bf16x2_to_float2(vr.y);
           v2f = bf16x2_to_float2(vr.z); v3f = bf16x2_to_float2(vr.w);
         }
-        const float vscale = F8 ? sks[kScaleEntries + j * p.num_kv_heads] : 1.f;
+        const float vscale = F8 ? sks[kEntries + j * p.num_kv_heads] : 1.f;
         float pj[G];
         if constexpr (G == 1) {
           pj[0] = sc[j];
@@ -841,8 +872,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
 size_t split_smem_bytes(int group) {
   return size_t(kStages) * kStageBytes + 2 * kStages * sizeof(uint64_t) +
          kStages * sizeof(StageDesc) + 32 * sizeof(float) +
-         size_t(kStages) * 2 * kScaleEntries * sizeof(float) +
-         size_t(kConsumerWarps) * kTokensPerWarp * group * sizeof(float);
+         size_t(kStages) * 2 * kScaleEntriesMax * sizeof(float) +
+         size_t(kConsumerWarps) * kTokensPerWarpMax * group * sizeof(float);
 }
 
 // both instances (bf16, fp8) of a group; the grid follows the bf16 one's
