@@ -57,6 +57,18 @@ def test_mixed_step_only_decodes_and_only_chunks():
         assert_close(out, ref, "mixed_edge")
 
 
+def test_mixed_step_with_empty_chunks():
+    # chunks with no new rows (with and without a cached prefix) among the
+    # round's chunks add no work and no output row
+    w, d = mixed_workload("mixed_empty", [4, 300], [0, 33, 0, 140], [10, 5, 0, 60], 16, 4, 16,
+                          seed=15)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    ref = prefill_step_reference(w, t["k_cache"], t["v_cache"], t["q"], t["key"], t["value"])
+    out, _ = run_mixed(w, d, t)
+    assert pkv.get_device_errors() == 0
+    assert_close(out, ref, "mixed_empty")
+
+
 def test_mixed_step_flags_a_decode_sequence_with_two_rows():
     w, d = mixed_workload("mixed_bad", [5, 9], [4], [2], 8, 2, 16, seed=12)
     t = {k: v.cuda() for k, v in w.tensors.items()}

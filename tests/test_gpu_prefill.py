@@ -42,6 +42,22 @@ def test_prefill_single_tile_no_prefix():
     check(W.prefill_workload("p_one", [128], [0], 32, 8, 16, seed=1))
 
 
+def test_prefill_empty_chunks_between_others():
+    # sequences with no new rows, with and without a cached prefix, between
+    # chunks: they claim no work item and own no output row
+    check(W.prefill_workload("p_empty", [0, 130, 0, 5, 0], [40, 100, 0, 3, 0], 16, 8, 16, seed=77))
+
+
+def test_prefill_with_no_rows_is_a_noop():
+    w = W.prefill_workload("p_none", [0, 0], [40, 0], 16, 8, 16, seed=78)
+    t = {k: v.cuda() for k, v in w.tensors.items()}
+    kc, vc = t["k_cache"].clone(), t["v_cache"].clone()
+    out = run_prefill_step(w, t)
+    torch.cuda.synchronize()
+    assert tuple(out.shape) == (0, 16, 128)
+    assert torch.equal(t["k_cache"], kc) and torch.equal(t["v_cache"], vc)
+
+
 @pytest.mark.parametrize("q_lens,prefixes", [
     ([1, 5, 128, 129, 300], [0, 17, 64, 3, 250]),
     ([64, 64], [1000, 1]),
