@@ -57,7 +57,7 @@ def test_decode_head_configurations(hkv, group):
 @pytest.mark.parametrize("hkv,group,bs", [(16, 1, 16), (3, 5, 32), (2, 16, 16), (1, 12, 8),
                                            (8, 4, 12), (4, 4, 6), (4, 4, 32), (32, 2, 16),
                                            (8, 3, 16), (16, 8, 16), (64, 1, 16), (2, 4, 3),
-                                           (1, 2, 8), (2, 8, 1), (1, 1, 5)])
+                                           (1, 2, 8), (2, 8, 1), (1, 1, 5), (1, 2, 1)])
 def test_decode_more_head_shapes(hkv, group, bs):
     # all-heads tcgen05 kernel when Hkv is 4, 8 or 16, G is 1, 2, 4 or 8 and
     # 128/Hkv divides the block size; per-head tcgen05 kernel for other block

@@ -50,7 +50,7 @@ def oracle_step_fp8(w, seq_ids, kc, vc, ks, vs, t):
 # else the CUDA-core kernel (2 x 4 at 16, 8 x 4 at 1, 1 x 8 at 4, 4 x 2 at 12)
 @pytest.mark.parametrize("hkv,group,bs", [(8, 4, 16), (8, 1, 16), (8, 2, 32), (4, 8, 32),
                                           (4, 2, 64), (8, 2, 256), (8, 8, 16), (2, 4, 16),
-                                          (8, 4, 1), (1, 8, 4), (4, 2, 12)])
+                                          (8, 4, 1), (1, 8, 4), (4, 2, 12), (1, 4, 1)])
 def test_fp8_store_and_decode_match_the_oracle(hkv, group, bs):
     lens = [1, 2, 15, 16, 17, 0, 300, 1025, 77, 2000]
     w = W.decode_workload(f"fp8_{hkv}x{group}_bs{bs}", lens, hkv * group, hkv, bs,
