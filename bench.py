@@ -886,10 +886,11 @@ def timed_after_clean_flush(fn, steps, device):
 
 def measure_small_blocks(device, steps):
     """Block sizes below a stage or tile (token-level paging among them): the
-    512-sequence decode (lognormal lengths, Hq 32 / Hkv 8; bf16 and fp8 E4M3)
-    and the 32 x 512 chunked prefill over the same prefixes as the prefill row,
-    at block sizes 16 (the reference), 8, 4 and 1; each call timed with CUDA
-    events after a clean L2 refill. Not part of the default run."""
+    512-sequence decode (lognormal lengths, Hq 32 / Hkv 8; bf16 and fp8 E4M3) at
+    block sizes 16, 8 and 1, and with Hq 8 / Hkv 2 at 16; the 32 x 512 chunked
+    prefill over the same prefixes as the prefill row at 16, 8, 4 and 1; each
+    call timed with CUDA events after a clean L2 refill. Not part of the
+    default run."""
     import torch
     import paged_kv_cache_86_gb300 as pkv
     from paged_kv_cache_86_gb300 import workloads as W
@@ -910,6 +911,22 @@ def measure_small_blocks(device, steps):
         res[f"fp8_decode_512seq_bs{bs}_ms"] = timed_after_clean_flush(
             lambda: pkv.paged_decode_fp8(q, kc, vc, ks, vs, bt, cl, w.scale), steps, device)
         del kc, vc, ks, vs
+    # two KV heads (Hq 8): the fp8 decode runs on the CUDA-core kernel at every
+    # block size, the bf16 one on the per-head tcgen05 kernel at 16
+    w = W.decode_workload("decode_512seq_hkv2_bs16", lens, 8, 2, 16, 86003, pool="fragmented",
+                          fill="device", device=device)
+    t = {k: v.to(device) for k, v in w.tensors.items() if k in ("q", "k_cache", "v_cache")}
+    bt = torch.from_numpy(w.block_tables).to(device)
+    cl = torch.from_numpy(w.context_lens).to(device)
+    res["decode_512seq_hkv2_bs16_ms"] = timed_after_clean_flush(
+        lambda: pkv.paged_decode(t["q"], t["k_cache"], t["v_cache"], bt, cl, w.scale), steps, device)
+    del t
+    kc, ks = W.fp8_pool(w.num_blocks, w.block_size, w.num_kv_heads, 7, device=device)
+    vc, vs = W.fp8_pool(w.num_blocks, w.block_size, w.num_kv_heads, 8, device=device)
+    q = torch.randn(w.num_seqs, 8, 128, device=device).to(torch.bfloat16)
+    res["fp8_decode_512seq_hkv2_bs16_ms"] = timed_after_clean_flush(
+        lambda: pkv.paged_decode_fp8(q, kc, vc, ks, vs, bt, cl, w.scale), steps, device)
+    del kc, vc, ks, vs
     prefixes = np.random.default_rng(86005 + 1000).integers(0, 3584 + 1, size=32)
     for bs in (16, 8, 4, 1):
         w = W.prefill_workload(f"prefill_32x512_bs{bs}", [512] * 32, prefixes, 32, 8, bs, 86005,
@@ -924,7 +941,8 @@ def measure_small_blocks(device, steps):
             steps, device)
         del t
     res["kernels"] = ("decode: all-heads tcgen05 at 16, CUDA-core with stages over several blocks "
-                      "below; prefill: TMA boxes at 16 and 8, rows gathered with cp.async below 8")
+                      "below; two KV heads: per-head tcgen05 (bf16) and CUDA-core (fp8) at 16; "
+                      "prefill: TMA boxes at 16 and 8, rows gathered with cp.async below 8")
     return res
 
 
