@@ -19,11 +19,14 @@
 //               of bytes however long or short the sequences are. Inside a
 //               CTA, one producer warp walks the range sequence by sequence
 //               and block by block and moves each run of up to
-//               16 KB / (Hkv*256 B) tokens of one physical block into a
-//               shared-memory stage with two bulk TMA copies (K and V; a
+//               16 KB / (Hkv * row bytes) tokens of one physical block into
+//               a shared-memory stage with two bulk TMA copies (K and V; a
 //               run of one block is contiguous across all KV heads in the
-//               [NB, bs, Hkv, D] layout). Eight consumer warps each take one
-//               KV head and an 8-token slice of the stage: the G query heads
+//               [NB, bs, Hkv, D] layout); a stage over blocks shorter than
+//               it takes one such pair of copies per block it touches. Eight
+//               consumer warps each take one KV head and an 8-token slice of
+//               the stage (16 with fp8 codes, whose rows are half the
+//               bytes and are expanded to fp32 as they are read): the G query heads
 //               of the group are scored together (K is read from shared
 //               memory once per group), scores are reduced across the 16
 //               lanes of a half-warp with a reduce-scatter of shuffles, the
@@ -52,7 +55,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 3;
 constexpr int kStageBytes = 32768;            // K half + V half
-constexpr int kTokensPerWarp = 8;             // stage tokens per consumer warp
+constexpr int kTokensPerWarp = 8;             // stage tokens per consumer warp (bf16; fp8 twice)
 constexpr int kMinRange = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
